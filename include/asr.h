@@ -1,0 +1,170 @@
+/*
+ * asr.h -- C ABI of the GB300 fused AdamW step with Philox-keyed stochastic
+ * rounding to bf16 (library: stochastic_rounding_gb300/libasr.so).
+ *
+ * What the operations compute is fixed by two pages:
+ *   "Add stochastic rounding and philox RNG helpers" (FlyDSL PR 907),
+ *       section Primitives -- stochastic rounding f32 -> bf16 and the Philox
+ *       4x32 counter-based generator that feeds it;
+ *   "adamw-sr", introduction and sections Method / Correctness -- the fused
+ *       decoupled-weight-decay Adam step with bf16 stochastic write-back, its
+ *       randomness keyed by (seed, step) and indexed by each element's global
+ *       parameter position, identical whole or in shards with a base_index.
+ *
+ * Conventions shared by every entry point
+ *   - Buffer pointers are DEVICE pointers (anything a kernel can dereference:
+ *     cudaMalloc / torch CUDA memory, managed memory), owned by the caller.
+ *     The library allocates no memory and keeps no state between calls apart
+ *     from a per-device cache of the SM count and occupancy.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising the host.  Buffers
+ *     must stay valid until the stream reaches the work.
+ *   - Arguments are checked before anything is launched.  A bad argument
+ *     returns ASR_ERR_INVALID_VALUE / ASR_ERR_UNSUPPORTED_DTYPE and launches
+ *     nothing.  A launch the CUDA runtime rejects returns ASR_ERR_CUDA (the
+ *     CUDA error code is then available from asr_last_cuda_error()).  Faults
+ *     that happen later on the GPU surface, as usual, at the next
+ *     synchronising CUDA call of the caller.
+ *   - n == 0 is a valid no-op (pointers may then be NULL).
+ *   - Any element alignment is accepted.  16-byte-aligned buffers and a
+ *     base_index that is a multiple of 4 take the vectorised fast path.
+ *   - Buffers of one call must not overlap each other (not checked).
+ *   - The library is thread-safe; calls on different streams may run
+ *     concurrently on disjoint buffers.
+ *
+ * Random bits.  Philox4x32-10 (Salmon et al., SC'11; the generator cuRAND
+ * calls Philox4_32_10): multipliers 0xD2511F53 and 0xCD9E8D57, Weyl
+ * increments 0x9E3779B9 and 0xBB67AE85.  For an element with global index i at
+ * (seed, step): key = (seed lo32, seed hi32), counter = ((i>>2) lo32,
+ * (i>>2) hi32, step, 0); the element uses word (i & 3) of the four output
+ * words, and only that word's low 16 bits.  One counter serves four
+ * consecutive elements.
+ *
+ * bf16 values are passed as their 16-bit patterns (uint16_t), bf16 = the top
+ * half of the binary32 pattern.
+ */
+#ifndef ASR_H
+#define ASR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers (same underlying type). */
+typedef struct CUstream_st *asr_stream_t;
+
+typedef enum {
+    ASR_OK = 0,
+    ASR_ERR_INVALID_VALUE = 1,      /* NULL pointer with n > 0, step == 0,
+                                       bad hyperparameter, bad count/size   */
+    ASR_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype / rounding enum out of range    */
+    ASR_ERR_CUDA = 3                /* the CUDA runtime rejected a call      */
+} asr_status;
+
+typedef enum { ASR_F32 = 0, ASR_BF16 = 1 } asr_dtype;
+
+/* How a bf16 parameter is written back.  Ignored for f32 parameters. */
+typedef enum {
+    ASR_ROUND_SR = 0,   /* stochastic: add 16 Philox bits, truncate (default) */
+    ASR_ROUND_RNE = 1   /* round to nearest, ties to even (biased baseline)   */
+} asr_rounding;
+
+/* AdamW hyperparameters of one step ("adamw-sr", Usage; Loshchilov and
+ * Hutter 2019).  Requirements: lr, eps, weight_decay finite and >= 0;
+ * 0 <= beta1, beta2 < 1; step >= 1 (the 1-based step count used both for the
+ * bias corrections and as Philox counter word 2). */
+typedef struct {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay;
+    uint32_t step;
+    uint32_t rounding;      /* asr_rounding */
+    uint64_t seed;
+} asr_adamw_hparams;
+
+/* The binary32 per-step scalars every element uses, each computed in binary64
+ * from the hyperparameters and rounded once:
+ *   b1 = beta1, b2 = beta2, eps, decay = 1 - lr*wd, omb1 = 1 - beta1,
+ *   omb2 = 1 - beta2, step_size = lr / (1 - beta1^step),
+ *   bc2s = sqrt(1 - beta2^step). */
+typedef struct {
+    float b1, b2, eps, decay, omb1, omb2, step_size, bc2s;
+} asr_adamw_scalars;
+
+/* One tensor (or one shard of a tensor) of a multi-tensor step. */
+typedef struct {
+    void *param;            /* n elements of param_dtype, updated in place   */
+    const void *grad;       /* n elements of grad_dtype, read only           */
+    float *exp_avg;         /* n binary32, first moment, updated in place    */
+    float *exp_avg_sq;      /* n binary32, second moment, updated in place   */
+    uint64_t n;
+    uint64_t base_index;    /* global parameter position of element 0        */
+    int32_t param_dtype;    /* asr_dtype */
+    int32_t grad_dtype;     /* asr_dtype */
+} asr_tensor_desc;
+
+/* Philox4x32-10 words ("Add stochastic rounding and philox RNG helpers",
+ * Primitives: philox_4x32(counter, key)).
+ * For j in [0, n_ctr): counter = ((ctr_base + j) lo32, (ctr_base + j) hi32,
+ * ctr2, ctr3), key = (seed lo32, seed hi32); out[4*j + w] = output word w.
+ * out: device, 4*n_ctr uint32 (caller-owned). */
+asr_status asr_philox4x32(uint32_t *out, uint64_t n_ctr, uint64_t ctr_base, uint32_t ctr2,
+                          uint32_t ctr3, uint64_t seed, asr_stream_t stream);
+
+/* Stochastic rounding f32 -> bf16 ("Add stochastic rounding and philox RNG
+ * helpers", Primitives: stochastic_round_bf16(x, rand)).
+ * out[j] = top 16 bits of (bits(x[j]) + (r_j & 0xFFFF)), where r_j is the
+ * Philox word of global index base_index + j at (seed, step), or rbits[j]
+ * when rbits is not NULL.  A NaN input gives (bits >> 16) | 0x0040 (still a
+ * NaN, quiet); +-Inf are unchanged; finite values that round past the largest
+ * bf16 become +-Inf.
+ * x: device, n binary32.  rbits: device, n uint32, or NULL.  out: device, n
+ * uint16 bf16 patterns. */
+asr_status asr_stochastic_round_bf16(const float *x, const uint32_t *rbits, uint16_t *out,
+                                     uint64_t n, uint64_t base_index, uint32_t step,
+                                     uint64_t seed, asr_stream_t stream);
+
+/* The per-step scalars of a hyperparameter set (host only; launches
+ * nothing).  Returns ASR_ERR_INVALID_VALUE for a set the step would reject. */
+asr_status asr_adamw_prepare(const asr_adamw_hparams *hp, asr_adamw_scalars *out);
+
+/* One fused AdamW step on one tensor or shard ("adamw-sr", introduction and
+ * Method).  For j in [0, n), with i = base_index + j and the scalars of
+ * asr_adamw_prepare, in binary32 with every operation rounded on its own in
+ * this order:
+ *   p1  = p*decay;  m' = b1*m + omb1*g;  v' = b2*v + omb2*(g*g);
+ *   den = sqrt(v')/bc2s + eps;  pn = p1 - step_size*(m'/den);
+ * then m <- m', v <- v', and p <- pn (f32 param) or the bf16 rounding of pn
+ * (stochastic with element i's Philox bits, or RNE, per hp->rounding).
+ * param: device, n elements of pdt.  grad: device, n elements of gdt.
+ * exp_avg / exp_avg_sq: device, n binary32 each.  hp: host. */
+asr_status asr_adamw_sr_step(void *param, int32_t pdt, const void *grad, int32_t gdt,
+                             float *exp_avg, float *exp_avg_sq, uint64_t n,
+                             uint64_t base_index, const asr_adamw_hparams *hp,
+                             asr_stream_t stream);
+
+/* The same step over many tensors in one grid-stride launch per dtype
+ * combination ("adamw-sr", Method: one global parameter position per
+ * element).  Bitwise equal to calling asr_adamw_sr_step on each descriptor in
+ * turn.  table: HOST array of n_tensors descriptors (read during the call
+ * only); n_tensors >= 0.  Descriptors with n == 0 are skipped. */
+asr_status asr_adamw_sr_multi_tensor(const asr_tensor_desc *table, int32_t n_tensors,
+                                     const asr_adamw_hparams *hp, asr_stream_t stream);
+
+/* Static description of a status code. */
+const char *asr_status_string(asr_status status);
+
+/* The CUDA runtime error code (cudaError_t as int) behind the calling
+ * thread's most recent ASR_ERR_CUDA, 0 if none. */
+int asr_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ASR_H */
