@@ -1,0 +1,340 @@
+"""Benchmark of the fused AdamW-SR step on the Llama-3-8B parameter set.
+
+One step = one fused AdamW step with stochastic bf16 write-back over all 291
+tensors (8,030,261,248 parameters; bf16 params and grads, f32 moments), i.e.
+one multi-tensor C-ABI call.  The working set (176.7 GB of traffic per step)
+is far larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line.  ``value`` is device-resident throughput (params/s over
+the timed steps, CUDA events); ``e2e`` repeats the measurement with the
+step's gradients copied from pinned host memory before, and the updated bf16
+params copied back after, every step.  ``--impl reference`` times the CPU
+oracle (single core) on a bounded sample of the same workload instead.
+Multi-GPU (torchrun): each rank updates its own full 8B-parameter shard of an
+N x 8B flat parameter vector (its base_index offset by rank), no collective on
+the data path: weak scaling.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "AdamW-SR step Gparams/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "Gparams/s"
+BYTES_PER_PARAM = 22          # bf16 p r/w (2+2), bf16 g r (2), f32 m r/w (4+4), f32 v r/w (4+4)
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+NORTH_STAR_PEAK_GBS = 8000.0
+KERNEL_SRC = os.path.join(ROOT, "stochastic_rounding_gb300", "csrc", "asr.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+CPU_SAMPLE_ELEMS = 1 << 24     # oracle sample per step (one core)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_sha():
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def traffic_per_param():
+    """DRAM bytes per parameter from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        if d.get("source_sha256") == source_sha():
+            return float(d["dram_bytes_per_param"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.remove(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+
+
+def cpu_oracle_sample(steps, sample_elems=CPU_SAMPLE_ELEMS, seed=0):
+    """Time the C oracle (one core) on a sample of the 8B workload: windows of
+    the 8B layout at their true base indices, bf16 p/g, f32 m/v.  Returns
+    (params/s per step list, description)."""
+    import numpy as np
+
+    import oracle
+    from stochastic_rounding_gb300 import workloads as W
+    o = oracle.get()
+    table = W.param_table(W.LLAMA_8B)
+    starts, _ = W.offsets(table)
+    big = [i for i, (_, n, norm) in enumerate(table) if not norm]
+    rng = np.random.default_rng(seed)
+    pieces = 8
+    per = sample_elems // pieces
+    windows = []
+    for t in rng.choice(big, pieces, replace=False):
+        s = int(rng.integers(0, table[t][1] - per)) & ~7
+        windows.append(int(starts[t]) + s)
+    hr = W.host_rng(seed, 1)
+    data = []
+    for base in windows:
+        data.append([W.to_bf16_bits(W.normal_f32(hr, per, 0.02)), W.to_bf16_bits(W.normal_f32(hr, per, 1e-3)),
+                     np.zeros(per, np.float32), np.zeros(per, np.float32), base])
+    rates = []
+    for step in range(1, steps + 1):
+        t0 = time.perf_counter()
+        for p, g, m, v, base in data:
+            o.adamw_step(p, g, m, v, step=step, seed=0, base_index=base, **HP)
+        dt = time.perf_counter() - t0
+        rates.append(pieces * per / dt)
+    desc = (f"{pieces} windows x {per} params of the Llama-3-8B layout (bf16 p/g, f32 m/v, true base "
+            f"indices), C oracle single thread, per step")
+    return rates, desc
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    rates, desc = cpu_oracle_sample(args.warmup + args.steps)
+    timed = rates[args.warmup:]
+    value = statistics.median(timed) / 1e9
+    ms = CPU_SAMPLE_ELEMS / (value * 1e9) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "llama3-8b AdamW-SR step, sampled for the CPU oracle",
+                   "params_per_step": CPU_SAMPLE_ELEMS, "param_dtype": "bf16", "grad_dtype": "bf16",
+                   "state_dtype": "f32"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from __graft_entry__ import build
+    build()
+    import stochastic_rounding_gb300 as asr
+    from stochastic_rounding_gb300 import _lib
+    from stochastic_rounding_gb300 import workloads as W
+
+    ps = W.DeviceParamSet(W.LLAMA_8B, device=dev, seed=rank, max_params=args.params)
+    tensors = ps.tensors()
+    # rank r owns parameters [r*N, (r+1)*N) of an N x 8B flat vector
+    offset = rank * ps.numel
+    table = _lib.make_table([(p, g, m, v, base + offset) for p, g, m, v, base in tensors])
+    stream = torch.cuda.Stream(device=dev)
+    n = ps.numel
+
+    def step(t):
+        asr.asr_adamw_sr_multi_tensor(table, step=t, seed=0, stream=stream, device=dev, **HP)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    t_global = 0
+    for _ in range(args.warmup):
+        t_global += 1
+        step(t_global)
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        all_start = torch.cuda.Event(enable_timing=True)
+        all_end = torch.cuda.Event(enable_timing=True)
+        all_start.record(stream)
+        for k in range(args.steps):
+            t_global += 1
+            starts[k].record(stream)
+            step(t_global)
+            ends[k].record(stream)
+        all_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = max_over_ranks(all_start.elapsed_time(all_end))
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    launch_ms = statistics.mean(per_launch_ms)
+    clock = clocks.summary()
+    launches = args.steps * 1                       # one multi-tensor launch per step
+
+    value = world * n * args.steps / (total_ms / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = BYTES_PER_PARAM * n / (launch_ms / 1e3) / 1e9
+    tpp = traffic_per_param()
+
+    # ---- end to end through the C ABI with host buffers
+    g_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    p_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    g_host.copy_(ps.g)
+    torch.cuda.synchronize(dev)
+    e_steps = max(1, min(args.steps, 3))
+    barrier()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(e_steps):
+            t_global += 1
+            ps.g.copy_(g_host, non_blocking=True)
+            step(t_global)
+            p_host.copy_(ps.p, non_blocking=True)
+        e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e_ms = max_over_ranks(e_start.elapsed_time(e_end))
+    e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
+
+    cpu = None
+    if rank == 0:
+        rates, desc = cpu_oracle_sample(steps=3)
+        cpu = {"value": statistics.median(rates) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": desc + ", median of 3 steps"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": ("llama3-8b" if not args.params else f"llama3-8b truncated to {n:,} params")
+                                   + f": fused AdamW-SR multi-tensor step, {len(tensors)} tensors, {n:,} params per GPU", "params_per_gpu": n, "tensors": len(tensors),
+                       "param_dtype": "bf16", "grad_dtype": "bf16", "state_dtype": "f32",
+                       "rounding": "stochastic (Philox4x32-10)", "bytes_per_param": BYTES_PER_PARAM,
+                       "l2": "inputs larger than L2 (176.7 GB moved per step)",
+                       "parallelism": f"shard{world}" if world > 1 else "single"},
+            "achieved_gbs": achieved, "frac_of_north_star_8tbs": achieved / NORTH_STAR_PEAK_GBS,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": tpp * n if tpp is not None else None,
+                         "kernel": "adamw_sr_kernel<bf16,bf16,SR,fast,512>",
+                         "launch_ms_mean": launch_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * n,
+                    "d2h_bytes_per_step": 2 * n, "steps": e_steps,
+                    "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host"},
+            "gpu_launches": launches,
+            "clocks": clock,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--params", type=int, default=0,
+                    help="keep only the tensors of the 8B layout that fit in this many params "
+                         "(a small case for profiling); 0 = the full set")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

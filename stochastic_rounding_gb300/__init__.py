@@ -1,0 +1,11 @@
+"""GB300-native fused AdamW step with Philox-keyed stochastic rounding to bf16.
+
+The computation lives in ``libasr.so`` (CUDA kernels for sm_103a behind a C
+ABI, declared in ``include/asr.h``); this package is its ctypes binding plus
+the synthetic workload definitions used to exercise it.
+"""
+from ._lib import (  # noqa: F401
+    ASR_BF16, ASR_F32, ASR_ROUND_RNE, ASR_ROUND_SR, AsrError, asr_adamw_prepare,
+    asr_adamw_sr_multi_tensor, asr_adamw_sr_step, asr_last_cuda_error, asr_philox4x32,
+    asr_status_string, asr_stochastic_round_bf16, lib, make_table,
+)

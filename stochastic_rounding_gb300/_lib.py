@@ -1,0 +1,237 @@
+"""ctypes binding of ``libasr.so`` with the C ABI's names.
+
+Argument marshalling only: tensors are checked (device, dtype, contiguity,
+size) and turned into device pointers, hyperparameters into the C struct, the
+current torch stream into a cudaStream_t.  Every step of the computation runs
+in the library's CUDA kernels.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libasr.so")
+
+ASR_OK, ASR_ERR_INVALID_VALUE, ASR_ERR_UNSUPPORTED_DTYPE, ASR_ERR_CUDA = 0, 1, 2, 3
+ASR_F32, ASR_BF16 = 0, 1
+ASR_ROUND_SR, ASR_ROUND_RNE = 0, 1
+
+# Every function the header declares.
+EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
+           "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
+           "asr_last_cuda_error")
+
+
+class AdamwHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("weight_decay", ctypes.c_double), ("step", ctypes.c_uint32),
+                ("rounding", ctypes.c_uint32), ("seed", ctypes.c_uint64)]
+
+
+class AdamwScalars(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_float) for k in
+                ("b1", "b2", "eps", "decay", "omb1", "omb2", "step_size", "bc2s")]
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("n", ctypes.c_uint64), ("base_index", ctypes.c_uint64),
+                ("param_dtype", ctypes.c_int32), ("grad_dtype", ctypes.c_int32)]
+
+
+class AsrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = f"{what}: {status_string(status)}"
+        if status == ASR_ERR_CUDA:
+            msg += f" (cudaError {lib().asr_last_cuda_error()})"
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with stochastic_rounding_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, u64, u32, i32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int32
+        L.asr_philox4x32.argtypes = [vp, u64, u64, u32, u32, u64, vp]
+        L.asr_stochastic_round_bf16.argtypes = [vp, vp, vp, u64, u64, u32, u64, vp]
+        L.asr_adamw_prepare.argtypes = [ctypes.POINTER(AdamwHparams), ctypes.POINTER(AdamwScalars)]
+        L.asr_adamw_sr_step.argtypes = [vp, i32, vp, i32, vp, vp, u64, u64,
+                                        ctypes.POINTER(AdamwHparams), vp]
+        L.asr_adamw_sr_multi_tensor.argtypes = [ctypes.POINTER(TensorDesc), i32,
+                                                ctypes.POINTER(AdamwHparams), vp]
+        for f in ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
+                  "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor"):
+            getattr(L, f).restype = ctypes.c_int
+        L.asr_status_string.argtypes = [ctypes.c_int]
+        L.asr_status_string.restype = ctypes.c_char_p
+        L.asr_last_cuda_error.argtypes = []
+        L.asr_last_cuda_error.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().asr_status_string(int(status)).decode()
+
+
+asr_status_string = status_string
+
+
+def asr_last_cuda_error() -> int:
+    return int(lib().asr_last_cuda_error())
+
+
+def _check(status: int, what: str):
+    if status != ASR_OK:
+        raise AsrError(status, what)
+
+
+def make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding="sr") -> AdamwHparams:
+    r = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE, ASR_ROUND_SR: ASR_ROUND_SR,
+         ASR_ROUND_RNE: ASR_ROUND_RNE}.get(rounding)
+    if r is None:
+        raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")
+    return AdamwHparams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                        int(step), r, int(seed) & (2**64 - 1))
+
+
+# ------------------------------------------------------------ tensor helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_ptr(t, name, dtypes, numel=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements; expected {numel}")
+    return t.data_ptr()
+
+
+def _stream_handle(device, stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dt(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return ASR_F32
+    if t.dtype in (torch.bfloat16, torch.int16):
+        return ASR_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ------------------------------------------------------------- entry points
+
+def asr_philox4x32(out, n_ctr: int, ctr_base: int, ctr2: int, ctr3: int, seed: int, stream=None):
+    """Philox4x32-10 words of ``n_ctr`` counters into ``out`` (int32/uint32
+    CUDA tensor of 4*n_ctr elements)."""
+    torch = _torch()
+    dts = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+    p = _dev_ptr(out, "out", dts, 4 * int(n_ctr))
+    with torch.cuda.device(out.device):
+        _check(lib().asr_philox4x32(p, int(n_ctr), int(ctr_base) & (2**64 - 1), int(ctr2) & 0xFFFFFFFF,
+                                    int(ctr3) & 0xFFFFFFFF, int(seed) & (2**64 - 1),
+                                    _stream_handle(out.device, stream)), "asr_philox4x32")
+    return out
+
+
+def asr_stochastic_round_bf16(x, out, *, base_index: int = 0, step: int = 0, seed: int = 0,
+                              rbits=None, stream=None):
+    """Stochastically round float32 ``x`` into ``out`` (bfloat16 or int16
+    CUDA tensor holding bf16 patterns)."""
+    torch = _torch()
+    n = x.numel()
+    px = _dev_ptr(x, "x", (torch.float32,))
+    po = _dev_ptr(out, "out", (torch.bfloat16, torch.int16), n)
+    pr = None
+    if rbits is not None:
+        dts = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+        pr = _dev_ptr(rbits, "rbits", dts, n)
+    with torch.cuda.device(x.device):
+        _check(lib().asr_stochastic_round_bf16(px, pr, po, n, int(base_index), int(step) & 0xFFFFFFFF,
+                                               int(seed) & (2**64 - 1), _stream_handle(x.device, stream)),
+               "asr_stochastic_round_bf16")
+    return out
+
+
+def asr_adamw_prepare(**hp) -> dict:
+    """The binary32 per-step scalars the library uses (host only)."""
+    h = make_hparams(**hp)
+    s = AdamwScalars()
+    _check(lib().asr_adamw_prepare(ctypes.byref(h), ctypes.byref(s)), "asr_adamw_prepare")
+    return {k: getattr(s, k) for k, _ in AdamwScalars._fields_}
+
+
+def asr_adamw_sr_step(param, grad, exp_avg, exp_avg_sq, *, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+                      weight_decay=0.0, step, seed=0, base_index: int = 0, rounding="sr", stream=None):
+    """One fused AdamW step in place on one tensor or shard."""
+    torch = _torch()
+    n = param.numel()
+    pp = _dev_ptr(param, "param", (torch.float32, torch.bfloat16, torch.int16))
+    pg = _dev_ptr(grad, "grad", (torch.float32, torch.bfloat16, torch.int16), n)
+    pm = _dev_ptr(exp_avg, "exp_avg", (torch.float32,), n)
+    pv = _dev_ptr(exp_avg_sq, "exp_avg_sq", (torch.float32,), n)
+    h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
+    with torch.cuda.device(param.device):
+        _check(lib().asr_adamw_sr_step(pp, _dt(param), pg, _dt(grad), pm, pv, n, int(base_index),
+                                       ctypes.byref(h), _stream_handle(param.device, stream)),
+               "asr_adamw_sr_step")
+
+
+def make_table(tensors: Sequence[Sequence]) -> ctypes.Array:
+    """Descriptor array from (param, grad, exp_avg, exp_avg_sq, base_index) tuples."""
+    torch = _torch()
+    arr = (TensorDesc * len(tensors))()
+    for i, (p, g, m, v, base) in enumerate(tensors):
+        n = p.numel()
+        arr[i] = TensorDesc(
+            _dev_ptr(p, f"param[{i}]", (torch.float32, torch.bfloat16, torch.int16)),
+            _dev_ptr(g, f"grad[{i}]", (torch.float32, torch.bfloat16, torch.int16), n),
+            _dev_ptr(m, f"exp_avg[{i}]", (torch.float32,), n),
+            _dev_ptr(v, f"exp_avg_sq[{i}]", (torch.float32,), n),
+            n, int(base), _dt(p), _dt(g))
+    return arr
+
+
+def asr_adamw_sr_multi_tensor(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+                              step, seed=0, rounding="sr", stream=None, device=None):
+    """One fused AdamW step over many tensors.  ``tensors`` is a sequence of
+    (param, grad, exp_avg, exp_avg_sq, base_index) tuples, or a descriptor
+    array made by ``make_table`` (then ``device`` names the CUDA device)."""
+    torch = _torch()
+    if isinstance(tensors, ctypes.Array):
+        table = tensors
+        dev = torch.device(device if device is not None else "cuda")
+    else:
+        table = make_table(tensors)
+        dev = tensors[0][0].device if len(tensors) else torch.device("cuda")
+    h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
+    with torch.cuda.device(dev):
+        _check(lib().asr_adamw_sr_multi_tensor(table, len(table), ctypes.byref(h),
+                                               _stream_handle(dev, stream)),
+               "asr_adamw_sr_multi_tensor")

@@ -123,3 +123,64 @@ def device_uniform_(t, gen, lo: float, hi: float, chunk: int = 1 << 27):
         tmp.mul_(hi - lo).add_(lo)
         flat[s:e].copy_(tmp)
     return t
+
+
+class DeviceParamSet:
+    """A decoder's parameter set laid out for one fused multi-tensor step.
+
+    Four flat device buffers -- bf16 params, bf16 grads, f32 first and second
+    moments -- hold every tensor back to back in model order, so tensor t is
+    the slice [start_t, start_t + n_t) of each buffer and its global parameter
+    position (base index) is start_t.  Every start is a multiple of 2048
+    elements, so every slice is 16-byte aligned.
+
+    Initial values: params ~N(0, 0.02) except RMSNorm weights = 1.0; grads
+    ~N(0, 1e-3); moments zero.  Drawn from torch's CUDA generator seeded with
+    ``seed``.
+    """
+
+    def __init__(self, shape: DecoderShape, device="cuda", seed: int = 0,
+                 p_std: float = 0.02, g_std: float = 1e-3, max_params: int = 0):
+        import torch
+        self.shape = shape
+        self.table = param_table(shape)
+        if max_params:
+            # the leading tensors of the layout, at most max_params in total
+            kept, total = [], 0
+            for entry in self.table:
+                if total + entry[1] > max_params:
+                    continue
+                kept.append(entry)
+                total += entry[1]
+            self.table = kept
+        starts, total = offsets(self.table)
+        self.starts = [int(s) for s in starts]
+        self.sizes = [n for _, n, _ in self.table]
+        self.numel = total
+        self.device = torch.device(device)
+        self.gen = torch.Generator(device=self.device)
+        self.gen.manual_seed(int(seed))
+        self.p = torch.empty(total, dtype=torch.bfloat16, device=self.device)
+        self.g = torch.empty(total, dtype=torch.bfloat16, device=self.device)
+        self.m = torch.zeros(total, dtype=torch.float32, device=self.device)
+        self.v = torch.zeros(total, dtype=torch.float32, device=self.device)
+        for (name, n, is_norm), s in zip(self.table, self.starts):
+            if is_norm:
+                self.p[s:s + n].fill_(1.0)
+            else:
+                device_normal_(self.p[s:s + n], self.gen, p_std)
+        self.g_std = g_std
+        self.new_grads()
+
+    def new_grads(self):
+        device_normal_(self.g, self.gen, self.g_std)
+
+    def tensors(self):
+        """(param, grad, exp_avg, exp_avg_sq, base_index) per tensor."""
+        out = []
+        for s, n in zip(self.starts, self.sizes):
+            out.append((self.p[s:s + n], self.g[s:s + n], self.m[s:s + n], self.v[s:s + n], s))
+        return out
+
+    def nbytes(self) -> int:
+        return self.numel * (2 + 2 + 4 + 4)

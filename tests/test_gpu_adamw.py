@@ -1,0 +1,265 @@
+"""GPU parity of the single-tensor fused AdamW-SR step through the C ABI
+against the oracle: bit-exact params (bf16 or f32) and f32 moments."""
+import numpy as np
+import pytest
+
+from gpu_util import assert_same_bits, dev, host, torch_cuda
+from stochastic_rounding_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+@pytest.fixture(scope="module")
+def asr():
+    torch_cuda()
+    from stochastic_rounding_gb300 import build
+    build.build()
+    import stochastic_rounding_gb300 as m
+    m.lib()
+    return m
+
+
+def _make(rng, n, pdt, gdt, states=True, pscale=0.02, gscale=1e-3):
+    p = W.normal_f32(rng, n, pscale)
+    g = W.normal_f32(rng, n, gscale)
+    if pdt == "bf16":
+        p = W.to_bf16_bits(p)
+    if gdt == "bf16":
+        g = W.to_bf16_bits(g)
+    if states:
+        m = W.normal_f32(rng, n, 1e-4)
+        v = np.abs(W.normal_f32(rng, n, 1e-6))
+    else:
+        m = np.zeros(n, np.float32)
+        v = np.zeros(n, np.float32)
+    return p, g, m, v
+
+
+def _step_both(asr, orc, h, d, **kw):
+    p, g, m, v = h
+    pd, gd, md, vd = d
+    base = kw.pop("base_index", 0)
+    asr.asr_adamw_sr_step(pd, gd, md, vd, base_index=base, **kw)
+    orc.adamw_step(p, g, m, v, base_index=base, rounding=0 if kw.get("rounding", "sr") == "sr" else 1,
+                   **{k: val for k, val in kw.items() if k != "rounding"})
+
+
+def _check(h, d, what):
+    for name, a, t in zip("pmv", (h[0], h[2], h[3]), (d[0], d[2], d[3])):
+        assert_same_bits(host(t), a, f"{what} {name}")
+
+
+def test_single_tensor_65536_bf16_10_steps(asr, orc):
+    """65,536 bf16 params ~N(0,0.02), bf16 grads ~N(0,1e-3) drawn per
+    (seed, step), m = v = 0, seed 0, 10 steps: bit-exact after every step."""
+    n, seed = 65536, 0
+    p = W.to_bf16_bits(W.normal_f32(W.host_rng(seed, 0), n, 0.02))
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    d = [dev(p), None, dev(m), dev(v)]
+    for step in range(1, 11):
+        g = W.to_bf16_bits(W.normal_f32(W.host_rng(seed, step), n, 1e-3))
+        d[1] = dev(g)
+        asr.asr_adamw_sr_step(d[0], d[1], d[2], d[3], step=step, seed=seed, **HP)
+        orc.adamw_step(p, g, m, v, step=step, seed=seed, **HP)
+        _check((p, g, m, v), d, f"step {step}")
+
+
+@pytest.mark.parametrize("pdt,gdt,rounding", [("bf16", "bf16", "sr"), ("bf16", "bf16", "rne"),
+                                              ("bf16", "f32", "sr"), ("bf16", "f32", "rne"),
+                                              ("f32", "bf16", "sr"), ("f32", "f32", "sr")])
+@pytest.mark.parametrize("base", [0, 5, 2**33 + 2, 2**40 + 3])
+def test_dtype_combinations_ragged(asr, orc, pdt, gdt, rounding, base):
+    n = 3 * 4096 + 13
+    rng = np.random.default_rng(hash((pdt, gdt, rounding, base)) % 2**32)
+    h = _make(rng, n, pdt, gdt)
+    d = [dev(a) for a in h]
+    for step in (1, 2, 3):
+        _step_both(asr, orc, h, d, step=step, seed=2**40 + 17, base_index=base, rounding=rounding, **HP)
+        _check(h, d, f"{pdt}/{gdt}/{rounding} base {base} step {step}")
+
+
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_unaligned_buffers(asr, orc, off):
+    """Buffers that start off a 16-byte boundary (slices) take the scalar
+    path and still match bit for bit; nothing outside the slice is written."""
+    import torch
+    n = 4096 * 2 + 77
+    rng = np.random.default_rng(off)
+    h = _make(rng, n + off, "bf16", "bf16")
+    full = [dev(a) for a in h]
+    d = [t[off:] for t in full]
+    hs = [a[off:].copy() for a in h]
+    guard = [host(t)[:off].copy() for t in full]
+    _step_both(asr, orc, hs, d, step=4, seed=3, base_index=10 + off, **HP)
+    _check(hs, d, f"offset {off}")
+    for g0, t in zip(guard, full):
+        assert np.array_equal(host(t)[:off], g0)
+    torch.cuda.synchronize()
+
+
+def test_small_and_boundary_sizes(asr, orc):
+    import torch
+    rng = np.random.default_rng(11)
+    for n in list(range(0, 34)) + [4095, 4096, 4097, 8191, 8193]:
+        for base in (0, 1, 3):
+            h = _make(rng, n, "bf16", "bf16")
+            # guard bands after the buffers
+            full = [dev(np.concatenate([a, np.full(9, 0x7E, a.dtype)])) for a in h]
+            d = [t[:n] for t in full]
+            _step_both(asr, orc, h, d, step=2, seed=5, base_index=base, **HP)
+            _check(h, d, f"n={n} base={base}")
+            for t, a in zip(full, h):
+                assert np.all(host(t)[n:] == 0x7E), f"n={n}: wrote past the end"
+    torch.cuda.synchronize()
+
+
+def test_special_values(asr, orc):
+    """Inf/NaN/zero/denormal params and grads; tiny and huge moments.  NaN
+    results compare as 'both NaN' (CPU and GPU NaN payloads differ)."""
+    rng = np.random.default_rng(12)
+    n = 4096 + 100
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-40, 3e38, -3e38, 1e-20], np.float32)
+    for pdt in ("bf16", "f32"):
+        p = W.normal_f32(rng, n, 1.0)
+        g = W.normal_f32(rng, n, 1.0)
+        p[rng.integers(0, n, 300)] = rng.choice(specials, 300)
+        g[rng.integers(0, n, 300)] = rng.choice(specials, 300)
+        m = W.normal_f32(rng, n, 1.0)
+        v = np.abs(W.normal_f32(rng, n, 1.0))
+        v[:50] = 0.0
+        m[:50] = 0.0
+        if pdt == "bf16":
+            p = W.to_bf16_bits(p)
+        h = [p, g, m, v]
+        d = [dev(a) for a in h]
+        for eps in (1e-8, 0.0):
+            _step_both(asr, orc, h, d, step=3, seed=8, lr=1e-2, beta1=0.9, beta2=0.999, eps=eps,
+                       weight_decay=0.1)
+            _check(h, d, f"specials {pdt} eps={eps}")
+
+
+def test_reproducible_and_keyed(asr):
+    """Same (seed, step) -> identical step; another seed or step changes the
+    bf16 params but not the moments."""
+    import torch
+    rng = np.random.default_rng(13)
+    h = _make(rng, 100000, "bf16", "bf16")
+    outs = {}
+    for key in ((1, 1), (1, 1), (2, 1), (1, 2)):
+        d = [dev(a) for a in h]
+        asr.asr_adamw_sr_step(d[0], d[1], d[2], d[3], step=key[1], seed=key[0], **HP)
+        outs.setdefault(key, []).append([host(t) for t in d])
+    torch.cuda.synchronize()
+    a, b = outs[(1, 1)]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    assert not np.array_equal(outs[(2, 1)][0][0], a[0])
+    assert np.array_equal(outs[(2, 1)][0][2], a[2])
+    assert not np.array_equal(outs[(1, 2)][0][0], a[0])
+
+
+def test_checkpoint_resume(asr):
+    """10 steps straight == 5 steps, copy every buffer to the host and back,
+    5 more steps (the generator is stateless, keyed by seed and step)."""
+    rng = np.random.default_rng(14)
+    n = 50000
+    h = _make(rng, n, "bf16", "bf16", states=False)
+    grads = [W.to_bf16_bits(W.normal_f32(rng, n, 1e-3)) for _ in range(10)]
+    a = [dev(x) for x in h]
+    for t in range(1, 11):
+        asr.asr_adamw_sr_step(a[0], dev(grads[t - 1]), a[2], a[3], step=t, seed=21, **HP)
+    b = [dev(x) for x in h]
+    for t in range(1, 6):
+        asr.asr_adamw_sr_step(b[0], dev(grads[t - 1]), b[2], b[3], step=t, seed=21, **HP)
+    saved = [host(x) for x in b]
+    b = [dev(x) for x in saved]
+    for t in range(6, 11):
+        asr.asr_adamw_sr_step(b[0], dev(grads[t - 1]), b[2], b[3], step=t, seed=21, **HP)
+    for x, y in zip(a, b):
+        if x is not None:
+            assert np.array_equal(host(x), host(y))
+
+
+def test_runs_on_the_given_stream(asr, orc):
+    import torch
+    rng = np.random.default_rng(15)
+    h = _make(rng, 1 << 20, "bf16", "bf16")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        d = [dev(a) for a in h]
+        asr.asr_adamw_sr_step(d[0], d[1], d[2], d[3], step=1, seed=1, **HP)
+    s.synchronize()
+    orc.adamw_step(h[0], h[1], h[2], h[3], step=1, seed=1, **HP)
+    _check(h, d, "side stream")
+
+
+def test_fp32_params_16m_100_steps(asr, orc):
+    """One f32 tensor of 16,777,216 elements ~N(0,0.02), f32 grads ~N(0,1e-3)
+    fresh per step, f32 moments, 100 steps: bit-exact with the oracle, and
+    within the page's 1e-4 of torch.optim.AdamW run on the same grads."""
+    import torch
+    n, steps = 16_777_216, 100
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(20240)
+    p = W.device_normal_(torch.empty(n, device="cuda"), gen, 0.02)
+    m = torch.zeros(n, device="cuda")
+    v = torch.zeros(n, device="cuda")
+    hp_ = host(p)
+    hm = np.zeros(n, np.float32)
+    hv = np.zeros(n, np.float32)
+    tp = torch.nn.Parameter(p.clone())
+    opt = torch.optim.AdamW([tp], lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                            weight_decay=HP["weight_decay"], foreach=False, fused=False)
+    g = torch.empty(n, device="cuda")
+    for step in range(1, steps + 1):
+        W.device_normal_(g, gen, 1e-3)
+        asr.asr_adamw_sr_step(p, g, m, v, step=step, seed=0, **HP)
+        tp.grad = g.clone()
+        opt.step()
+        orc.adamw_step(hp_, host(g), hm, hv, step=step, seed=0, **HP)
+        if step in (1, 2, 50, 100):
+            assert_same_bits(host(p), hp_, f"f32 p step {step}")
+            assert_same_bits(host(m), hm, f"f32 m step {step}")
+            assert_same_bits(host(v), hv, f"f32 v step {step}")
+    diff = float((p.double() - tp.detach().double()).abs().max())
+    assert diff < 1e-4, f"max |p - torch AdamW| = {diff}"
+
+
+@pytest.mark.parametrize("states", ["zero", "random"])
+def test_shard_invariance_268m(asr, orc, states):
+    """268,435,456 bf16 params ~U(-1,1), bf16 grads ~N(0,1e-2), seed 1234,
+    step 7: the whole tensor and 8 contiguous shards with their base_index
+    give bitwise-equal results; sampled windows match the oracle."""
+    import torch
+    n, shards = 268_435_456, 8
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    p0 = W.device_uniform_(torch.empty(n, dtype=torch.bfloat16, device="cuda"), gen, -1.0, 1.0)
+    g = W.device_normal_(torch.empty(n, dtype=torch.bfloat16, device="cuda"), gen, 1e-2)
+    if states == "zero":
+        m0 = torch.zeros(n, device="cuda")
+        v0 = torch.zeros(n, device="cuda")
+    else:
+        m0 = W.device_normal_(torch.empty(n, device="cuda"), gen, 1e-3)
+        v0 = W.device_normal_(torch.empty(n, device="cuda"), gen, 1e-4).abs_()
+    rng = np.random.default_rng(7)
+    win = [(0, 4096), (n - 4096, 4096)] + [(int(s), 4096) for s in rng.integers(0, n - 4096, 14)]
+    before = [(host(p0[s:s + L]), host(g[s:s + L]), host(m0[s:s + L]), host(v0[s:s + L])) for s, L in win]
+    pw, mw, vw = p0.clone(), m0.clone(), v0.clone()
+    asr.asr_adamw_sr_step(pw, g, mw, vw, step=7, seed=1234, **HP)
+    ps, ms, vs = p0.clone(), m0.clone(), v0.clone()
+    L = n // shards
+    for k in range(shards):
+        sl = slice(k * L, (k + 1) * L)
+        asr.asr_adamw_sr_step(ps[sl], g[sl], ms[sl], vs[sl], base_index=k * L, step=7, seed=1234, **HP)
+    torch.cuda.synchronize()
+    assert torch.equal(pw.view(torch.int16), ps.view(torch.int16))
+    assert torch.equal(mw.view(torch.int32), ms.view(torch.int32))
+    assert torch.equal(vw.view(torch.int32), vs.view(torch.int32))
+    for (s, Ln), (hp0, hg, hm, hv) in zip(win, before):
+        orc.adamw_step(hp0, hg, hm, hv, step=7, seed=1234, base_index=s, **HP)
+        assert_same_bits(host(pw[s:s + Ln]), hp0, f"window {s} p")
+        assert_same_bits(host(mw[s:s + Ln]), hm, f"window {s} m")
+        assert_same_bits(host(vw[s:s + Ln]), hv, f"window {s} v")

@@ -1,0 +1,134 @@
+"""GPU parity of the multi-tensor launch: bitwise equal to per-tensor calls
+and to the oracle; Llama-shaped parameter sets checked on sampled windows."""
+import numpy as np
+import pytest
+
+from gpu_util import assert_same_bits, dev, host, pick_windows, torch_cuda
+from stochastic_rounding_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+@pytest.fixture(scope="module")
+def asr():
+    torch_cuda()
+    from stochastic_rounding_gb300 import build
+    build.build()
+    import stochastic_rounding_gb300 as m
+    m.lib()
+    return m
+
+
+def _random_set(rng, count, max_n, offsets=(0, 0, 0, 1, 3)):
+    """Host arrays and device slices of ``count`` tensors with mixed dtypes,
+    some starting off a 16-byte boundary, bases cumulative with gaps."""
+    host_t, base = [], 5
+    for i in range(count):
+        n = int(rng.integers(0, max_n))
+        pdt = rng.choice(["bf16", "f32"])
+        gdt = rng.choice(["bf16", "f32"])
+        off = int(rng.choice(offsets))
+        p = W.normal_f32(rng, n + off, 0.02)
+        g = W.normal_f32(rng, n + off, 1e-3)
+        if pdt == "bf16":
+            p = W.to_bf16_bits(p)
+        if gdt == "bf16":
+            g = W.to_bf16_bits(g)
+        m = W.normal_f32(rng, n + off, 1e-4)
+        v = np.abs(W.normal_f32(rng, n + off, 1e-6))
+        host_t.append(([p, g, m, v], off, base))
+        base += n + int(rng.integers(0, 3))
+    return host_t
+
+
+def _dev_set(host_t):
+    out = []
+    for arrs, off, base in host_t:
+        ts = [dev(a)[off:] for a in arrs]
+        out.append((ts[0], ts[1], ts[2], ts[3], base))
+    return out
+
+
+@pytest.mark.parametrize("rounding", ["sr", "rne"])
+def test_multi_equals_per_tensor_and_oracle(asr, orc, rounding):
+    import torch
+    rng = np.random.default_rng(21 if rounding == "sr" else 22)
+    hs = _random_set(rng, 37, 20000)
+    a = _dev_set(hs)
+    b = _dev_set(hs)
+    for step in (1, 2):
+        asr.asr_adamw_sr_multi_tensor(a, step=step, seed=2**35 + 1, rounding=rounding, **HP)
+        for p, g, m, v, base in b:
+            asr.asr_adamw_sr_step(p, g, m, v, base_index=base, step=step, seed=2**35 + 1,
+                                  rounding=rounding, **HP)
+        for arrs, off, base in hs:
+            p, g, m, v = (x[off:].copy() for x in arrs)
+            orc.adamw_step(p, g, m, v, step=step, seed=2**35 + 1, base_index=base,
+                           rounding=0 if rounding == "sr" else 1, **HP)
+            for x, y in zip(arrs, (p, g, m, v)):
+                x[off:] = y
+    torch.cuda.synchronize()
+    for i, ((arrs, off, base), ta, tb) in enumerate(zip(hs, a, b)):
+        for k in (0, 2, 3):
+            assert np.array_equal(host(ta[k]).view(np.uint8), host(tb[k]).view(np.uint8)), \
+                f"tensor {i}: multi-tensor differs from per-tensor calls"
+            assert_same_bits(host(ta[k]), arrs[k][off:], f"tensor {i} buffer {k}")
+
+
+def test_more_tensors_than_one_launch_holds(asr, orc):
+    """1,100 small tensors (more than one launch's table) in one call."""
+    import torch
+    rng = np.random.default_rng(23)
+    hs = _random_set(rng, 1100, 300, offsets=(0,))
+    a = _dev_set(hs)
+    asr.asr_adamw_sr_multi_tensor(a, step=3, seed=4, **HP)
+    torch.cuda.synchronize()
+    for i, ((arrs, off, base), t) in enumerate(zip(hs, a)):
+        p, g, m, v = (x.copy() for x in arrs)
+        orc.adamw_step(p, g, m, v, step=3, seed=4, base_index=base, **HP)
+        assert_same_bits(host(t[0]), p, f"tensor {i} p")
+        assert_same_bits(host(t[2]), m, f"tensor {i} m")
+        assert_same_bits(host(t[3]), v, f"tensor {i} v")
+
+
+def _check_windows(asr, orc, ps, table, windows, step, seed):
+    """One multi-tensor step, with the windows checked against the oracle."""
+    import torch
+    before = []
+    for t, s, n in windows:
+        a = ps.starts[t] + s
+        before.append([host(x[a:a + n]) for x in (ps.p, ps.g, ps.m, ps.v)])
+    asr.asr_adamw_sr_multi_tensor(table, step=step, seed=seed, device=ps.device, **HP)
+    torch.cuda.synchronize()
+    for (t, s, n), (p, g, m, v) in zip(windows, before):
+        a = ps.starts[t] + s
+        orc.adamw_step(p, g, m, v, step=step, seed=seed, base_index=a, **HP)
+        assert_same_bits(host(ps.p[a:a + n]), p, f"{ps.table[t][0]}[{s}:{s + n}] p step {step}")
+        assert_same_bits(host(ps.m[a:a + n]), m, f"{ps.table[t][0]}[{s}:{s + n}] m step {step}")
+        assert_same_bits(host(ps.v[a:a + n]), v, f"{ps.table[t][0]}[{s}:{s + n}] v step {step}")
+
+
+@pytest.mark.parametrize("shape,steps,checked", [(W.LLAMA_1B, 20, (1, 2, 20)), (W.LLAMA_8B, 10, (1, 10))],
+                         ids=["llama-1.5B-147t-20steps", "llama3-8B-291t-10steps"])
+def test_llama_param_set_sampled(asr, orc, shape, steps, checked):
+    """The Llama-shaped sets in one multi-tensor launch per step: norm tensors
+    whole, every other tensor's head, tail and two random unaligned windows
+    checked against the oracle at the listed steps."""
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    ps = W.DeviceParamSet(shape, seed=0)
+    table = _lib.make_table(ps.tensors())
+    rng = np.random.default_rng(31)
+    windows = pick_windows(rng, ps.sizes, per_tensor=2, length=2048)
+    for step in range(1, steps + 1):
+        if step > 1:
+            ps.new_grads()
+        if step in checked:
+            _check_windows(asr, orc, ps, table, windows, step, seed=0)
+        else:
+            asr.asr_adamw_sr_multi_tensor(table, step=step, seed=0, device=ps.device, **HP)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(ps.p[:1 << 20].float()).all())
+    del ps
+    torch.cuda.empty_cache()
