@@ -163,6 +163,20 @@ const char *asr_status_string(asr_status status);
  * thread's most recent ASR_ERR_CUDA, 0 if none. */
 int asr_last_cuda_error(void);
 
+/* Sticky error bits raised on the device by the current device's kernels,
+ * read and cleared.  Bit 0 (1): a pipeline wait inside a kernel gave up
+ * after its time limit (2 s); the kernel then left the affected tiles
+ * unfinished and returned instead of hanging.  Waits for `stream`, then
+ * stores the bits (0 = no error) in *bits (host). */
+asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream);
+
+/* Diagnostic (no counterpart on the pages): launches one thread that waits,
+ * with the kernels' bounded-wait routine and a limit of limit_ns
+ * (1 .. 2e9 ns), on a barrier nothing arrives on.  The wait gives up, the
+ * kernel returns, and the next asr_take_device_error reports bit 0.  Used to
+ * show that a stuck pipeline ends with a status instead of a hang. */
+asr_status asr_selftest_wait_timeout(uint64_t limit_ns, asr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ ASR_ROUND_SR, ASR_ROUND_RNE = 0, 1
 # Every function the header declares.
 EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
            "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
-           "asr_last_cuda_error")
+           "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout")
 
 
 class AdamwHparams(ctypes.Structure):
@@ -76,6 +76,10 @@ def lib() -> ctypes.CDLL:
             getattr(L, f).restype = ctypes.c_int
         L.asr_status_string.argtypes = [ctypes.c_int]
         L.asr_status_string.restype = ctypes.c_char_p
+        L.asr_selftest_wait_timeout.argtypes = [u64, vp]
+        L.asr_selftest_wait_timeout.restype = ctypes.c_int
+        L.asr_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        L.asr_take_device_error.restype = ctypes.c_int
         L.asr_last_cuda_error.argtypes = []
         L.asr_last_cuda_error.restype = ctypes.c_int
         _lib = L
@@ -91,6 +95,26 @@ asr_status_string = status_string
 
 def asr_last_cuda_error() -> int:
     return int(lib().asr_last_cuda_error())
+
+
+def asr_take_device_error(stream=None, device=None) -> int:
+    """Read and clear the device-side error bits (0 = none); waits for the stream."""
+    torch = _torch()
+    dev = torch.device(device if device is not None else "cuda")
+    bits = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        _check(lib().asr_take_device_error(ctypes.byref(bits), _stream_handle(dev, stream)),
+               "asr_take_device_error")
+    return int(bits.value)
+
+
+def asr_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None, device=None):
+    """Launch the bounded-wait self-test (a wait that must give up)."""
+    torch = _torch()
+    dev = torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(dev):
+        _check(lib().asr_selftest_wait_timeout(int(limit_ns), _stream_handle(dev, stream)),
+               "asr_selftest_wait_timeout")
 
 
 def _check(status: int, what: str):

@@ -37,9 +37,18 @@ namespace {
 
 // ------------------------------------------------------------------ config
 
-constexpr int kThreads = 256;               // threads per CTA
+#ifndef ASR_THREADS
+#define ASR_THREADS 256
+#endif
+#ifndef ASR_UNROLL
+#define ASR_UNROLL 2
+#endif
+#ifndef ASR_MIN_BLOCKS
+#define ASR_MIN_BLOCKS 1
+#endif
+constexpr int kThreads = ASR_THREADS;       // threads per CTA
 constexpr int kVec = 8;                     // elements per unit (one 16 B bf16 vector)
-constexpr int kUnroll = 2;                  // units per thread per tile
+constexpr int kUnroll = ASR_UNROLL;         // units per thread per tile
 constexpr int kTile = kThreads * kVec * kUnroll;   // 4096 elements per tile
 constexpr int kCapLarge = 512;              // descriptors per multi-tensor launch
 constexpr int kCapSmall = 1;                // single-tensor launch
@@ -189,7 +198,14 @@ __device__ __forceinline__ void unit_words(uint64_t base, uint64_t e, uint32_t s
 // Streaming 128-bit accesses: every byte is touched once, so keep it out of
 // L1 and mark it evict-first in L2.
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+#ifndef ASR_STORE_CS
+#define ASR_STORE_CS 1
+#endif
+#if ASR_STORE_CS
 __device__ __forceinline__ void st_stream(void *p, uint4 v) { __stcs(reinterpret_cast<uint4 *>(p), v); }
+#else
+__device__ __forceinline__ void st_stream(void *p, uint4 v) { *reinterpret_cast<uint4 *>(p) = v; }
+#endif
 
 // ------------------------------------------------------------ AdamW unit
 
@@ -324,7 +340,7 @@ __device__ __forceinline__ void scalar_unit(const TensorEntry &T, uint64_t e, co
 // Persistent grid-stride kernel over the tiles of every tensor in the table.
 // FAST: every tensor has 16-byte-aligned buffers and base % 4 == 0.
 template <int PT, int GT, int RM, bool FAST, int CAP>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, ASR_MIN_BLOCKS)
 adamw_sr_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P)
 {
     int t = 0;
@@ -356,6 +372,308 @@ adamw_sr_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constan
                 }
             }
         }
+    }
+}
+
+// --------------------------------------------- bulk-copy pipelined kernel
+//
+// The same step, with the loads taken off the registers: a producer warp
+// streams every tile's p, g, m and v into a ring of shared-memory stages with
+// cp.async.bulk (the Blackwell/Hopper bulk-copy engine; completion counted on
+// an mbarrier), while consumer warps compute from shared memory and store
+// their results straight to global memory.  With several 48 KB stages in
+// flight per SM the kernel keeps far more bytes outstanding than register
+// occupancy allows.
+//
+// Every mbarrier wait is bounded by a %globaltimer limit; a wait that gives
+// up sets a bit in g_device_error, the thread leaves its loop, and the
+// producer still waits (bounded) for the copies it issued before exiting.
+
+#ifndef ASR_TMA_STAGES
+#define ASR_TMA_STAGES 4
+#endif
+#ifndef ASR_TMA_CONSUMER_WARPS
+#define ASR_TMA_CONSUMER_WARPS 20
+#endif
+#ifndef ASR_TMA_SMEM_KB
+#define ASR_TMA_SMEM_KB 200
+#endif
+#ifndef ASR_TMA_EVICT_FIRST
+#define ASR_TMA_EVICT_FIRST 1
+#endif
+#ifndef ASR_TMA_TILE
+#define ASR_TMA_TILE 5120
+#endif
+constexpr int kTmaTile = ASR_TMA_TILE;
+constexpr int kTmaConsumerWarps = ASR_TMA_CONSUMER_WARPS;
+constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
+constexpr int kTmaThreads = kTmaConsumers + 32;        // + one producer warp
+constexpr int kTmaUnits = kTmaTile / kVec / kTmaConsumers;   // units per consumer thread per tile
+static_assert(kTmaUnits >= 1 && kTmaUnits * kTmaConsumers * kVec == kTmaTile, "tile must split evenly");
+constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: a healthy wait takes microseconds
+
+constexpr uint32_t kErrWaitTimeout = 1u;
+
+__device__ unsigned int g_device_error = 0;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the phase with the given parity has completed, for at most
+// limit_ns.  Returns false (and raises the device error bit) on timeout.
+// A second guard caps the number of polls, so the wait ends even if the
+// timer did not advance.
+constexpr uint32_t kWaitMaxPolls = 1u << 26;
+
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t polls = 0; !mbar_test(bar, parity); ++polls) {
+        if (global_ns() - t0 > limit_ns || polls >= kWaitMaxPolls) {
+            atomicOr(&g_device_error, kErrWaitTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_test(bar, parity)) return true;      // fast path: already complete
+    return mbar_wait_bounded(bar, parity, limit_ns);
+}
+
+// Diagnostic: one thread waits, with the given limit, on a barrier that
+// nothing arrives on, so the bounded wait must give up and raise the error
+// bit.  Shows that a stuck pipeline ends with a readable status.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(b, 0, limit_ns);
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy)
+{
+#if ASR_TMA_EVICT_FIRST
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+#else
+    (void)policy;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+#endif
+}
+
+template <int PT, int GT>
+struct TmaStage {
+    static constexpr int kPBytes = kTmaTile * (PT == ASR_BF16 ? 2 : 4);
+    static constexpr int kGBytes = kTmaTile * (GT == ASR_BF16 ? 2 : 4);
+    static constexpr int kMBytes = kTmaTile * 4;
+    static constexpr int kBytes = kPBytes + kGBytes + 2 * kMBytes;
+    // as many stages as fit in the shared-memory budget, at most ASR_TMA_STAGES
+    static constexpr int kFit = ASR_TMA_SMEM_KB * 1024 / kBytes;
+    static constexpr int kStages = kFit < ASR_TMA_STAGES ? kFit : ASR_TMA_STAGES;
+    static_assert(kStages >= 2, "need at least two stages");
+    static constexpr int kSmem = kStages * kBytes + 2 * kStages * 8 + kTmaConsumerWarps * 4;
+};
+
+// Locate tile `tile` of the table, advancing the cursor t.
+template <int CAP>
+__device__ __forceinline__ void find_tile(const AdamTable<CAP> &tab, uint64_t tile, int &t, uint64_t &off,
+                                          uint32_t &cnt)
+{
+    while (tile >= tab.t[t].tile_end) ++t;
+    const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
+    off = (tile - first) * static_cast<uint64_t>(kTmaTile);
+    const uint64_t rest = tab.t[t].n - off;
+    cnt = rest < static_cast<uint64_t>(kTmaTile) ? static_cast<uint32_t>(rest) : static_cast<uint32_t>(kTmaTile);
+}
+
+// All tensors FAST (16-byte-aligned buffers, base % 4 == 0); tile size kTmaTile.
+template <int PT, int GT, int RM, int CAP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P,
+                    uint64_t limit_ns)
+{
+    using S = TmaStage<PT, GT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bars = sbase + S::kStages * S::kBytes;      // full[s] then empty[s]
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (S::kStages + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kTmaConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == kTmaConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane != 0) return;
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        int t = 0;
+        uint32_t k = 0;
+        for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+            const int s = static_cast<int>(k % S::kStages);
+            const uint32_t use = k / S::kStages;
+            if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
+            uint64_t off;
+            uint32_t cnt;
+            find_tile(tab, tile, t, off, cnt);
+            const TensorEntry &T = tab.t[t];
+            const uint32_t c8 = cnt & ~7u;
+            const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
+            const uint32_t mb = c8 * 4u;
+            mbar_arrive_expect_tx(full(s), pb + gb + 2 * mb);
+            if (c8) {
+                const uint32_t dst = sbase + s * S::kBytes;
+                bulk_load(dst, static_cast<const unsigned char *>(T.p) + off * (PT == ASR_BF16 ? 2 : 4), pb,
+                          full(s), policy);
+                bulk_load(dst + S::kPBytes, static_cast<const unsigned char *>(T.g) + off * (GT == ASR_BF16 ? 2 : 4),
+                          gb, full(s), policy);
+                bulk_load(dst + S::kPBytes + S::kGBytes, T.m + off, mb, full(s), policy);
+                bulk_load(dst + S::kPBytes + S::kGBytes + S::kMBytes, T.v + off, mb, full(s), policy);
+            }
+        }
+        // Every copy this thread issued must land before the CTA may exit:
+        // wait (bounded) for the last use of each stage.
+        const uint32_t issued = k;
+        for (int s = 0; s < S::kStages; ++s) {
+            if (static_cast<uint32_t>(s) >= issued) break;
+            const uint32_t last_use = (issued - 1 - s) / S::kStages;
+            mbar_wait(full(s), last_use & 1u, limit_ns);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ct = threadIdx.x;            // 0 .. kTmaConsumers-1
+    const uint32_t dep_slot = bars + 16u * S::kStages + 4u * warp;   // one word per consumer warp
+    int t = 0;
+    uint32_t k = 0;
+    for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % S::kStages);
+        const uint32_t use = k / S::kStages;
+        if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
+        uint64_t off;
+        uint32_t cnt;
+        find_tile(tab, tile, t, off, cnt);
+        const TensorEntry &T = tab.t[t];
+        const uint32_t c8 = cnt & ~7u;
+        const unsigned char *st = smem + s * S::kBytes;
+        VecUnit<PT, GT> u[kTmaUnits];
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8) {
+                if (PT == ASR_BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 2);
+                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 4);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(st + e * 4 + 16);
+                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
+                    u[j].p[4] = b.x; u[j].p[5] = b.y; u[j].p[6] = b.z; u[j].p[7] = b.w;
+                }
+                const unsigned char *gs = st + S::kPBytes;
+                if (GT == ASR_BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 2);
+                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 4);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(gs + e * 4 + 16);
+                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
+                    u[j].g[4] = b.x; u[j].g[5] = b.y; u[j].g[6] = b.z; u[j].g[7] = b.w;
+                }
+                const float4 *ms = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + e * 4);
+                const float4 *vs = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + S::kMBytes + e * 4);
+                const float4 m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1];
+                u[j].m[0] = m0.x; u[j].m[1] = m0.y; u[j].m[2] = m0.z; u[j].m[3] = m0.w;
+                u[j].m[4] = m1.x; u[j].m[5] = m1.y; u[j].m[6] = m1.z; u[j].m[7] = m1.w;
+                u[j].v[0] = v0.x; u[j].v[1] = v0.y; u[j].v[2] = v0.z; u[j].v[3] = v0.w;
+                u[j].v[4] = v1.x; u[j].v[5] = v1.y; u[j].v[6] = v1.z; u[j].v[7] = v1.w;
+            }
+        }
+        // Hand the stage back only once this warp's shared-memory loads have
+        // returned (the next bulk copy into the stage would otherwise race
+        // with a load still queued): every lane folds one register of each
+        // 128-bit load into `dep` and stores it; in-order issue holds that
+        // store, and so the warp barrier and the release after it, until
+        // every folded load is back.
+        uint32_t dep = 0;
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8)
+                dep ^= u[j].p[0] ^ u[j].g[0] ^ __float_as_uint(u[j].m[0]) ^ __float_as_uint(u[j].m[4]) ^
+                       __float_as_uint(u[j].v[0]) ^ __float_as_uint(u[j].v[4]) ^
+                       (PT == ASR_BF16 ? 0u : u[j].p[4]) ^ (GT == ASR_BF16 ? 0u : u[j].g[4]);
+        }
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dep_slot), "r"(dep) : "memory");
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(empty(s));
+        }
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
+        }
+        // a ragged end of a tensor (< 8 elements) goes through the scalar path
+        if (c8 < cnt && ct == (c8 / kVec) % kTmaConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
     }
 }
 
@@ -551,10 +869,47 @@ bool desc_fast(const asr_tensor_desc &d)
            (d.base_index & 3u) == 0;
 }
 
+#ifndef ASR_USE_TMA
+#define ASR_USE_TMA 1
+#endif
+
+// Dynamic shared memory opt-in and persistent grid of the bulk-copy kernel,
+// cached per (device, kernel).
+template <typename K>
+asr_status tma_grid(K kernel, int smem, int *grid)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const uint64_t key = (static_cast<uint64_t>(dev) << 48) ^ reinterpret_cast<uintptr_t>(kernel) ^ 1u;
+    {
+        std::lock_guard<std::mutex> lk(g_grid_mu);
+        auto it = g_grid_cache.find(key);
+        if (it != g_grid_cache.end()) {
+            *grid = it->second;
+            return ASR_OK;
+        }
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kTmaThreads, smem);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm < 1) per_sm = 1;
+    *grid = sms * per_sm;
+    std::lock_guard<std::mutex> lk(g_grid_mu);
+    g_grid_cache[key] = *grid;
+    return ASR_OK;
+}
+
 template <int PT, int GT, int RM, bool FAST, int CAP>
 asr_status launch_group(const asr_tensor_desc *const *descs, int count, const AdamParams &P, cudaStream_t stream)
 {
     static_assert(CAP >= 1, "");
+    constexpr bool kTma = FAST && ASR_USE_TMA;
+    constexpr uint64_t tile = kTma ? kTmaTile : kTile;
     AdamTable<CAP> tab;
     std::memset(&tab, 0, sizeof(tab));
     uint64_t tiles = 0;
@@ -567,18 +922,28 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
         T.v = d.exp_avg_sq;
         T.n = d.n;
         T.base = d.base_index;
-        tiles += (d.n + kTile - 1) / kTile;
+        tiles += (d.n + tile - 1) / tile;
         T.tile_end = tiles;
     }
     tab.total_tiles = tiles;
     tab.count = count;
     if (tiles == 0) return ASR_OK;
-    auto kernel = adamw_sr_kernel<PT, GT, RM, FAST, CAP>;
     int grid = 0;
-    asr_status st = persistent_grid(kernel, &grid);
-    if (st != ASR_OK) return st;
-    if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
-    kernel<<<grid, kThreads, 0, stream>>>(tab, P);
+    asr_status st;
+    if (kTma) {
+        auto kernel = adamw_sr_tma_kernel<PT, GT, RM, CAP>;
+        const int smem = TmaStage<PT, GT>::kSmem;
+        st = tma_grid(kernel, smem, &grid);
+        if (st != ASR_OK) return st;
+        if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
+        kernel<<<grid, kTmaThreads, smem, stream>>>(tab, P, kWaitLimitNs);
+    } else {
+        auto kernel = adamw_sr_kernel<PT, GT, RM, FAST, CAP>;
+        st = persistent_grid(kernel, &grid);
+        if (st != ASR_OK) return st;
+        if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
+        kernel<<<grid, kThreads, 0, stream>>>(tab, P);
+    }
     return check_launch();
 }
 
@@ -679,6 +1044,26 @@ const char *asr_status_string(asr_status status)
 }
 
 int asr_last_cuda_error(void) { return g_last_cuda_error; }
+
+asr_status asr_selftest_wait_timeout(uint64_t limit_ns, asr_stream_t stream)
+{
+    if (limit_ns == 0 || limit_ns > kWaitLimitNs) return ASR_ERR_INVALID_VALUE;
+    wait_timeout_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+    return check_launch();
+}
+
+asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream)
+{
+    if (!bits) return ASR_ERR_INVALID_VALUE;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int h = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_device_error, sizeof(h), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *bits = h;
+    return ASR_OK;
+}
 
 asr_status asr_adamw_prepare(const asr_adamw_hparams *hp, asr_adamw_scalars *out)
 {

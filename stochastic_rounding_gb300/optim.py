@@ -1,0 +1,152 @@
+"""``AdamWSR``: a torch optimizer over the fused AdamW-SR kernels.
+
+"adamw-sr", section Usage: a drop-in for ``torch.optim.AdamW`` whose states
+are float32, whose parameters may be float32 or bfloat16 (bf16 ones written
+back by stochastic rounding, no fp32 master copy) and whose gradients may be
+float32 or bfloat16.  Section Method: the rounding bits are keyed by
+(seed, step) and indexed by each element's global parameter position.
+
+Global positions: the parameters, in the order the optimizer was given them
+(all groups, in group order), are laid end to end; a parameter's base index
+is the number of elements before it.  Every step of a group is one
+multi-tensor launch (per device and per distinct step count).
+"""
+from __future__ import annotations
+
+from typing import Dict, List
+
+import torch
+
+from . import _lib
+
+
+class AdamWSR(torch.optim.Optimizer):
+    """AdamW with stochastic rounding of bf16 parameters.
+
+    Arguments follow ``torch.optim.AdamW`` (``lr``, ``betas``, ``eps``,
+    ``weight_decay``) plus ``seed`` (64-bit key of the rounding stream) and
+    ``rounding`` (``"sr"``, or ``"rne"`` for round-to-nearest-even, the
+    biased baseline).  Parameters must be contiguous CUDA tensors of float32
+    or bfloat16; gradients dense float32 or bfloat16.
+    """
+
+    def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
+                 weight_decay: float = 1e-2, *, seed: int = 0, rounding: str = "sr"):
+        if not 0.0 <= lr:
+            raise ValueError(f"Invalid learning rate: {lr}")
+        if not 0.0 <= eps:
+            raise ValueError(f"Invalid epsilon value: {eps}")
+        if not 0.0 <= betas[0] < 1.0:
+            raise ValueError(f"Invalid beta parameter at index 0: {betas[0]}")
+        if not 0.0 <= betas[1] < 1.0:
+            raise ValueError(f"Invalid beta parameter at index 1: {betas[1]}")
+        if not 0.0 <= weight_decay:
+            raise ValueError(f"Invalid weight_decay value: {weight_decay}")
+        if rounding not in ("sr", "rne"):
+            raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")
+        if not 0 <= int(seed) < 2**64:
+            raise ValueError("seed must fit in 64 bits")
+        defaults = dict(lr=lr, betas=tuple(betas), eps=eps, weight_decay=weight_decay,
+                        seed=int(seed), rounding=rounding)
+        super().__init__(params, defaults)
+        self._assign_positions()
+        self._table_cache: Dict[tuple, object] = {}
+
+    def _assign_positions(self):
+        pos = 0
+        self._base: Dict[int, int] = {}
+        for group in self.param_groups:
+            for p in group["params"]:
+                if id(p) in self._base:
+                    continue
+                self._base[id(p)] = pos
+                pos += p.numel()
+
+    def add_param_group(self, param_group):
+        super().add_param_group(param_group)
+        if hasattr(self, "_base"):
+            self._assign_positions()
+
+    def base_index(self, p: torch.Tensor) -> int:
+        """Global parameter position of element 0 of ``p``."""
+        return self._base[id(p)]
+
+    @staticmethod
+    def _check(p: torch.Tensor):
+        if p.device.type != "cuda":
+            raise ValueError("AdamWSR parameters must live on a CUDA device")
+        if p.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError(f"AdamWSR supports float32 and bfloat16 parameters, not {p.dtype}")
+        if not p.is_contiguous():
+            raise ValueError("AdamWSR parameters must be contiguous")
+        g = p.grad
+        if g.is_sparse:
+            raise RuntimeError("AdamWSR does not support sparse gradients")
+        if g.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError(f"AdamWSR supports float32 and bfloat16 gradients, not {g.dtype}")
+        if not g.is_contiguous() or g.shape != p.shape or g.device != p.device:
+            raise ValueError("gradient must be contiguous, on the parameter's device and of its shape")
+
+    @torch.no_grad()
+    def step(self, closure=None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        for group in self.param_groups:
+            beta1, beta2 = group["betas"]
+            # (device, step) -> list of (p, g, m, v, base)
+            batches: Dict[tuple, List[tuple]] = {}
+            for p in group["params"]:
+                if p.grad is None:
+                    continue
+                self._check(p)
+                state = self.state[p]
+                if len(state) == 0:
+                    state["step"] = 0
+                    state["exp_avg"] = torch.zeros_like(p, dtype=torch.float32,
+                                                        memory_format=torch.contiguous_format)
+                    state["exp_avg_sq"] = torch.zeros_like(p, dtype=torch.float32,
+                                                           memory_format=torch.contiguous_format)
+                state["step"] = int(state["step"]) + 1
+                key = (p.device, state["step"])
+                batches.setdefault(key, []).append(
+                    (p, p.grad, state["exp_avg"], state["exp_avg_sq"], self._base[id(p)]))
+            for (device, step), entries in batches.items():
+                table = self._table(entries)
+                _lib.asr_adamw_sr_multi_tensor(
+                    table, lr=group["lr"], beta1=beta1, beta2=beta2, eps=group["eps"],
+                    weight_decay=group["weight_decay"], step=step, seed=group["seed"],
+                    rounding=group["rounding"], device=device)
+        return loss
+
+    def _table(self, entries):
+        """Descriptor table for these tensors, reused while every pointer,
+        size and dtype is unchanged (gradients are often reallocated)."""
+        key = tuple((p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(), p.numel(), base,
+                     p.dtype, g.dtype) for p, g, m, v, base in entries)
+        table = self._table_cache.get(key)
+        if table is None:
+            if len(self._table_cache) > 64:
+                self._table_cache.clear()
+            table = _lib.make_table(entries)
+            self._table_cache[key] = table
+        return table
+
+    def load_state_dict(self, state_dict):
+        """Like torch's, but the moments stay float32: torch's loader casts
+        floating-point state to the parameter's dtype, which for a bf16
+        parameter would round the moments to bf16."""
+        from itertools import chain
+        super().load_state_dict(state_dict)
+        saved_ids = chain.from_iterable(g["params"] for g in state_dict["param_groups"])
+        params = chain.from_iterable(g["params"] for g in self.param_groups)
+        id_map = dict(zip(saved_ids, params))
+        for pid, st in state_dict["state"].items():
+            p = id_map[pid]
+            for k in ("exp_avg", "exp_avg_sq"):
+                if k in st:
+                    self.state[p][k] = st[k].to(device=p.device, dtype=torch.float32, copy=True)
+            if "step" in self.state[p]:
+                self.state[p]["step"] = int(self.state[p]["step"])
+        self._table_cache.clear()

@@ -263,3 +263,72 @@ def test_shard_invariance_268m(asr, orc, states):
         assert_same_bits(host(pw[s:s + Ln]), hp0, f"window {s} p")
         assert_same_bits(host(mw[s:s + Ln]), hm, f"window {s} m")
         assert_same_bits(host(vw[s:s + Ln]), hv, f"window {s} v")
+
+
+def test_no_device_error_after_steps(asr):
+    """Ordinary steps never trip a pipeline wait limit."""
+    rng = np.random.default_rng(16)
+    h = _make(rng, 3 * 4096 * 152 + 5, "bf16", "bf16")
+    d = [dev(a) for a in h]
+    asr.asr_take_device_error()
+    for step in (1, 2, 3):
+        asr.asr_adamw_sr_step(d[0], d[1], d[2], d[3], step=step, seed=1, **HP)
+    assert asr.asr_take_device_error() == 0
+
+
+def test_bounded_wait_gives_up_with_a_status(asr):
+    """A wait on a barrier nothing arrives on ends after its limit (1 ms) and
+    reports bit 0; the context stays usable (a step still runs afterwards)."""
+    import time
+    asr.asr_take_device_error()
+    t0 = time.perf_counter()
+    asr.asr_selftest_wait_timeout(1_000_000)
+    bits = asr.asr_take_device_error()
+    assert bits == 1
+    assert time.perf_counter() - t0 < 10.0
+    assert asr.asr_take_device_error() == 0
+    rng = np.random.default_rng(17)
+    h = _make(rng, 5000, "bf16", "bf16")
+    d = [dev(a) for a in h]
+    asr.asr_adamw_sr_step(d[0], d[1], d[2], d[3], step=1, seed=1, **HP)
+    assert asr.asr_take_device_error() == 0
+
+
+@pytest.mark.parametrize("pdt,gdt,n,steps", [("bf16", "bf16", 48_000_000 + 4096 * 3 + 8, 24),
+                                             ("f32", "f32", 16_777_216, 40),
+                                             ("bf16", "f32", 20_000_000, 16)])
+def test_pipeline_matches_plain_path_every_step(asr, pdt, gdt, n, steps):
+    """Race check for the bulk-copy pipeline: the same inputs updated through
+    the pipelined kernel (16-byte-aligned buffers) and through the plain
+    kernel (the same data one element off alignment, which forces the scalar
+    path) with equal global indices must agree bit for bit after every step."""
+    import torch
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(n + steps)
+    pt = torch.bfloat16 if pdt == "bf16" else torch.float32
+    gt = torch.bfloat16 if gdt == "bf16" else torch.float32
+
+    def pair(dtype, fill):
+        a = torch.empty(n, dtype=dtype, device="cuda")
+        fill(a)
+        b_full = torch.empty(n + 1, dtype=dtype, device="cuda")
+        b = b_full[1:]
+        b.copy_(a)
+        return a, b
+
+    pa, pb = pair(pt, lambda t: W.device_normal_(t, gen, 0.02))
+    ma, mb = pair(torch.float32, lambda t: W.device_normal_(t, gen, 1e-4))
+    va, vb = pair(torch.float32, lambda t: W.device_normal_(t, gen, 1e-6).abs_())
+    ga, gb = pair(gt, lambda t: W.device_normal_(t, gen, 1e-3))
+    assert pa.data_ptr() % 16 == 0 and pb.data_ptr() % 16 != 0
+    asr.asr_take_device_error()
+    for step in range(1, steps + 1):
+        W.device_normal_(ga, gen, 1e-3)
+        gb.copy_(ga)
+        asr.asr_adamw_sr_step(pa, ga, ma, va, base_index=4096, step=step, seed=11, **HP)
+        asr.asr_adamw_sr_step(pb, gb, mb, vb, base_index=4096, step=step, seed=11, **HP)
+        iv = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)  # noqa: E731
+        assert torch.equal(iv(pa), iv(pb)), f"params differ at step {step}"
+        assert torch.equal(ma.view(torch.int32), mb.view(torch.int32)), f"m differs at step {step}"
+        assert torch.equal(va.view(torch.int32), vb.view(torch.int32)), f"v differs at step {step}"
+    assert asr.asr_take_device_error() == 0
