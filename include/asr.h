@@ -156,6 +156,36 @@ asr_status asr_adamw_sr_step(void *param, int32_t pdt, const void *grad, int32_t
 asr_status asr_adamw_sr_multi_tensor(const asr_tensor_desc *table, int32_t n_tensors,
                                      const asr_adamw_hparams *hp, asr_stream_t stream);
 
+/* The same step as asr_adamw_sr_multi_tensor, for callers that must not
+ * allocate device memory: code running where another allocator owns the
+ * device's memory (a framework's pooling allocator, a memory-capped job), so
+ * that a raw cudaMalloc would fail or escape that allocator's accounting, and
+ * code that must not pay for an allocation inside a training step.  The
+ * pages have no counterpart: this is a packaging variant of the step.
+ *
+ * Its scratch, the descriptor table the kernel walks, is staged in a
+ * library-owned static device array of ASR_STATIC_TABLE_MAX descriptors
+ * (224 KB, held on every device that loads the library until the process
+ * exits) instead of the launch parameters, so one launch per dtype group
+ * covers up to ASR_STATIC_TABLE_MAX tensors.  Results are bitwise equal to
+ * asr_adamw_sr_multi_tensor.
+ *   - n_tensors > ASR_STATIC_TABLE_MAX returns ASR_ERR_INVALID_VALUE before
+ *     anything is launched; otherwise the checks of the other entry points.
+ *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
+ *     routine; host staging uses fixed static buffers.
+ *   - The first call on a device does that device's set-up (the array's
+ *     device address, via cudaGetSymbolAddress with the device current, and
+ *     the kernels' launch shapes); make that first call before any stream
+ *     capture.
+ *   - The table is copied from host memory on `stream`, so the call returns
+ *     only after the work already queued on `stream` has finished.
+ *   - Every call reuses the one array and leaves its table there: calls whose
+ *     kernels overlap on the GPU (other streams, other host threads) race on
+ *     it.  Each call rewrites the part it uses; nothing has to start at zero. */
+#define ASR_STATIC_TABLE_MAX 4096
+asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_t n_tensors,
+                                            const asr_adamw_hparams *hp, asr_stream_t stream);
+
 /* Static description of a status code. */
 const char *asr_status_string(asr_status status);
 

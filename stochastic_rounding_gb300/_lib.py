@@ -22,7 +22,9 @@ ASR_ROUND_SR, ASR_ROUND_RNE = 0, 1
 # Every function the header declares.
 EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
            "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
-           "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout")
+           "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout",
+           "asr_adamw_sr_multi_tensor_static")
+ASR_STATIC_TABLE_MAX = 4096
 
 
 class AdamwHparams(ctypes.Structure):
@@ -71,8 +73,11 @@ def lib() -> ctypes.CDLL:
                                         ctypes.POINTER(AdamwHparams), vp]
         L.asr_adamw_sr_multi_tensor.argtypes = [ctypes.POINTER(TensorDesc), i32,
                                                 ctypes.POINTER(AdamwHparams), vp]
+        L.asr_adamw_sr_multi_tensor_static.argtypes = [ctypes.POINTER(TensorDesc), i32,
+                                                       ctypes.POINTER(AdamwHparams), vp]
         for f in ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
-                  "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor"):
+                  "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor",
+                  "asr_adamw_sr_multi_tensor_static"):
             getattr(L, f).restype = ctypes.c_int
         L.asr_status_string.argtypes = [ctypes.c_int]
         L.asr_status_string.restype = ctypes.c_char_p
@@ -259,3 +264,24 @@ def asr_adamw_sr_multi_tensor(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, 
         _check(lib().asr_adamw_sr_multi_tensor(table, len(table), ctypes.byref(h),
                                                _stream_handle(dev, stream)),
                "asr_adamw_sr_multi_tensor")
+
+
+def asr_adamw_sr_multi_tensor_static(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+                                     weight_decay=0.0, step, seed=0, rounding="sr", stream=None,
+                                     device=None):
+    """Allocation-free variant of ``asr_adamw_sr_multi_tensor`` for callers
+    that may not allocate device memory: the descriptor table is staged in a
+    library-owned device array (at most ASR_STATIC_TABLE_MAX tensors), and
+    calls must not overlap on the GPU.  Same arguments, same results."""
+    torch = _torch()
+    if isinstance(tensors, ctypes.Array):
+        table = tensors
+        dev = torch.device(device if device is not None else "cuda")
+    else:
+        table = make_table(tensors)
+        dev = tensors[0][0].device if len(tensors) else torch.device("cuda")
+    h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
+    with torch.cuda.device(dev):
+        _check(lib().asr_adamw_sr_multi_tensor_static(table, len(table), ctypes.byref(h),
+                                                      _stream_handle(dev, stream)),
+               "asr_adamw_sr_multi_tensor_static")

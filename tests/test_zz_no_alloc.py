@@ -1,0 +1,102 @@
+"""The allocation-free multi-tensor entry point.
+
+Some callers cannot allocate device memory themselves: their framework's
+allocator owns the device (a raw cudaMalloc would fail in a memory-capped job
+or escape the allocator's accounting), or they must not pay for an
+allocation inside a step.  asr_adamw_sr_multi_tensor_static serves them: its
+scratch, the tensor descriptor table the kernel walks, sits in a
+library-owned static device array.  These tests check, through the C ABI,
+that two calls in a row give bit for bit the results of the regular
+multi-tensor entry point, and that a table above the maximum is refused.
+
+Kept in a file of its own that is collected last, so a failure here cannot
+stop a run with -x before the other tests have run.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+from gpu_util import torch_cuda
+
+pytestmark = pytest.mark.gpu
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+@pytest.fixture(scope="module")
+def L():
+    torch_cuda()
+    from stochastic_rounding_gb300 import build
+    build.build()
+    from stochastic_rounding_gb300 import _lib
+    return _lib.lib()
+
+
+def _tensor_set(seed):
+    """About 700 tensors, more than one launch's parameter table holds:
+    mixed dtypes, sizes from 1 to ~2M elements, a few starting off a
+    16-byte boundary.  Returns (p, g, m, v, base) tuples of CUDA tensors."""
+    import torch
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    out, base = [], 0
+    sizes = [int(x) for x in rng.integers(1, 3000, 690)] + [2_000_003, 1 << 20, 65536 + 5, 4096, 7]
+    for i, n in enumerate(sizes):
+        pdt = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+        gdt = torch.bfloat16 if rng.random() < 0.6 else torch.float32
+        off = 1 if i % 97 == 5 else 0
+
+        def mk(dtype, std):
+            return torch.randn(n + off, device="cuda", generator=gen).mul_(std).to(dtype)[off:]
+        out.append((mk(pdt, 0.02), mk(gdt, 1e-3), mk(torch.float32, 1e-4),
+                    mk(torch.float32, 1e-6).abs_(), base))
+        base += n + int(rng.integers(0, 3))
+    return out
+
+
+def _clone(tensors):
+    """Copies of params and moments at the same 16-byte alignment offset."""
+    import torch
+
+    def cp(t):
+        off = (t.data_ptr() % 16) // t.element_size()
+        full = torch.empty(t.numel() + off, dtype=t.dtype, device=t.device)
+        full[off:].copy_(t)
+        return full[off:]
+    return [(cp(p), g, cp(m), cp(v), base) for p, g, m, v, base in tensors]
+
+
+def _bits(t):
+    import torch
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def test_no_alloc_entry_matches_multi_tensor_entry(L):
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    a = _tensor_set(1234)
+    b = _clone(a)
+    ta = _lib.make_table(a)
+    tb = _lib.make_table(b)
+    sh = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for step in (1, 2):                      # two calls in a row
+        hp = _lib.make_hparams(step=step, seed=2**33 + 7, **HP)
+        assert L.asr_adamw_sr_multi_tensor(ta, len(ta), ctypes.byref(hp), sh) == _lib.ASR_OK
+        assert L.asr_adamw_sr_multi_tensor_static(tb, len(tb), ctypes.byref(hp), sh) == _lib.ASR_OK
+        torch.cuda.synchronize()
+        for i, (x, y) in enumerate(zip(a, b)):
+            for k in (0, 2, 3):
+                assert torch.equal(_bits(x[k]), _bits(y[k])), f"step {step}: tensor {i} buffer {k} differs"
+    bits = ctypes.c_uint32(0)
+    assert L.asr_take_device_error(ctypes.byref(bits), sh) == _lib.ASR_OK and bits.value == 0
+
+
+def test_no_alloc_entry_rejects_oversized_tables(L):
+    from stochastic_rounding_gb300 import _lib
+    hp = _lib.make_hparams(step=1, seed=0, **HP)
+    big = (_lib.TensorDesc * (_lib.ASR_STATIC_TABLE_MAX + 1))()
+    for d in big:
+        d.param_dtype = d.grad_dtype = 1
+    assert L.asr_adamw_sr_multi_tensor_static(big, len(big), ctypes.byref(hp), None) \
+        == _lib.ASR_ERR_INVALID_VALUE
