@@ -306,7 +306,7 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": tpp * n if tpp is not None else None,
-                         "kernel": "adamw_sr_kernel<bf16,bf16,SR,fast,512>",
+                         "kernel": "adamw_sr_tma_kernel<bf16,bf16,SR,512>",
                          "launch_ms_mean": launch_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * n,
