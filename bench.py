@@ -10,7 +10,8 @@ is far larger than L2, so no flush is needed between steps.
 Prints one JSON line.  ``value`` is device-resident throughput (params/s over
 the timed steps, CUDA events); ``e2e`` repeats the measurement with the
 step's gradients copied from pinned host memory before, and the updated bf16
-params copied back after, every step.  ``--impl reference`` times the CPU
+params copied back after, every step (chunks of consecutive tensors pipelined
+over three streams so both copy directions overlap the compute).  ``--impl reference`` times the CPU
 oracle (single core) on a bounded sample of the same workload instead.
 Multi-GPU (torchrun): each rank updates its own full 8B-parameter shard of an
 N x 8B flat parameter vector (its base_index offset by rank), no collective on
@@ -169,6 +170,29 @@ def cpu_oracle_sample(steps, sample_elems=CPU_SAMPLE_ELEMS, seed=0):
     return rates, desc
 
 
+def e2e_chunks(tensors, offset, max_params=1 << 28):
+    """Consecutive tensors grouped into chunks of at most max_params (a larger
+    tensor is a chunk of its own).  Each chunk is a contiguous range [lo, hi)
+    of the flat buffers with its own descriptor table."""
+    from stochastic_rounding_gb300 import _lib
+    groups, group, count = [], [], 0
+    for t in tensors:
+        n_t = t[0].numel()
+        if group and count + n_t > max_params:
+            groups.append(group)
+            group, count = [], 0
+        group.append(t)
+        count += n_t
+    if group:
+        groups.append(group)
+    res = []
+    for grp in groups:
+        lo = grp[0][4]
+        hi = grp[-1][4] + grp[-1][0].numel()
+        res.append((lo, hi, _lib.make_table([(p, g, m, v, base + offset) for p, g, m, v, base in grp])))
+    return res
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -263,23 +287,54 @@ def run_gpu(args):
     achieved = BYTES_PER_PARAM * n / (launch_ms / 1e3) / 1e9
     tpp = traffic_per_param()
 
-    # ---- end to end through the C ABI with host buffers
+    # ---- end to end through the C ABI with host buffers: every step copies
+    # the grads in from pinned host memory and the updated bf16 params back
+    # out.  Chunks of consecutive tensors (contiguous ranges of the flat
+    # buffers) are pipelined over three streams: H2D of chunk c+1 and D2H of
+    # chunk c-1 overlap the multi-tensor call on chunk c.
     g_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
     p_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
     g_host.copy_(ps.g)
+    chunks = e2e_chunks(tensors, offset)
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    done_cmp = [None] * len(chunks)          # compute of chunk c finished (grads free)
+    done_out = [None] * len(chunks)          # params of chunk c copied out (params free)
     torch.cuda.synchronize(dev)
-    e_steps = max(1, min(args.steps, 3))
+    e_steps = max(1, args.steps)
+    launches_e2e = 0
     barrier()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e_start.record(stream)
-        for _ in range(e_steps):
-            t_global += 1
-            ps.g.copy_(g_host, non_blocking=True)
-            step(t_global)
-            p_host.copy_(ps.p, non_blocking=True)
-        e_end.record(stream)
+    e_start.record(stream)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    for _ in range(e_steps):
+        t_global += 1
+        for c, (lo, hi, ctable) in enumerate(chunks):
+            ev_in = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                if done_cmp[c] is not None:
+                    s_in.wait_event(done_cmp[c])
+                ps.g[lo:hi].copy_(g_host[lo:hi], non_blocking=True)
+                ev_in.record(s_in)
+            stream.wait_event(ev_in)
+            if done_out[c] is not None:
+                stream.wait_event(done_out[c])
+            asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
+            launches_e2e += 1
+            ev_c = torch.cuda.Event()
+            ev_c.record(stream)
+            done_cmp[c] = ev_c
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c)
+                p_host[lo:hi].copy_(ps.p[lo:hi], non_blocking=True)
+                ev_o = torch.cuda.Event()
+                ev_o.record(s_out)
+            done_out[c] = ev_o
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
+    e_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
@@ -310,8 +365,10 @@ def run_gpu(args):
                          "launch_ms_mean": launch_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * n,
-                    "d2h_bytes_per_step": 2 * n, "steps": e_steps,
-                    "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host"},
+                    "d2h_bytes_per_step": 2 * n, "steps": e_steps, "chunks": len(chunks),
+                    "gpu_launches": launches_e2e,
+                    "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host; "
+                            "chunks of consecutive tensors pipelined over three streams"},
             "gpu_launches": launches,
             "clocks": clock,
         }

@@ -171,3 +171,17 @@ def test_sr_large_unbiased(asr, orc):
     got = host(out[torch.from_numpy(idx).cuda()])
     want = np.array([orc.sr_bf16(xv, orc.element_word(int(i), 1, 77)) for i in idx], np.uint16)
     assert_same_bits(got, want, "sampled", nan_equal=False)
+
+
+def test_hardware_sr_conversion_equals_add_and_truncate(tmp_path):
+    """cvt.rs.bf16x2.f32, which the stand-alone rounding op uses for non-NaN
+    pairs, gives the add-and-truncate result in both lanes for every non-NaN
+    binary32 pattern, with every 1024th random value and the two values at
+    each input's round-up threshold (the full 2^16 sweep: `cvt_rs_sweep 1`)."""
+    torch_cuda()
+    exe = os.path.join(str(tmp_path), "cvt_rs_sweep")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-o", exe,
+                    os.path.join(HERE, "cvt_rs_sweep.cu")], check=True)
+    r = subprocess.run([exe, "1024"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert " 0 mismatches" in r.stdout
