@@ -378,6 +378,56 @@ def run_gpu(args):
     return 0
 
 
+def run_gemm(args):
+    """The tcgen05 GEMM with the stochastic-rounding epilogue (and with the
+    round-to-nearest epilogue, and torch.matmul = cuBLAS, for context) on
+    one m x n x k problem: TFLOP/s by CUDA events over the timed launches,
+    against the measured bf16 tensor peak."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    import stochastic_rounding_gb300 as asr
+    m, n, k = args.gemm
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    a = torch.randn(m, k, device=dev, generator=g).to(torch.bfloat16)
+    b = torch.randn(n, k, device=dev, generator=g).to(torch.bfloat16)
+    c = torch.empty(m, n, device=dev, dtype=torch.bfloat16)
+    flops = 2.0 * m * n * k
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    t_sr = timed(lambda: asr.asr_gemm_bf16_sr(a, b, c, rounding="sr", step=1, seed=0))
+    t_rn = timed(lambda: asr.asr_gemm_bf16_sr(a, b, c, rounding="rne"))
+    t_cublas = timed(lambda: torch.matmul(a, b.t()))
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        peak, kind = 1900.0, "fallback"
+    tf = flops / (t_sr / 1e3) / 1e12
+    line = {"metric": "bf16 GEMM with stochastic-rounding epilogue TFLOP/s", "value": tf, "unit": "TFLOP/s",
+            "ms": t_sr, "config": {"workload": f"gemm {m}x{n}x{k} bf16, f32 accumulate, C = A.B^T"},
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_kind": kind},
+            "rne_epilogue_tflops": flops / (t_rn / 1e3) / 1e12,
+            "cublas_torch_matmul_tflops": flops / (t_cublas / 1e3) / 1e12,
+            "steps": args.steps, "warmup": args.warmup}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -387,7 +437,11 @@ def main():
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the tensors of the 8B layout that fit in this many params "
                          "(a small case for profiling); 0 = the full set")
+    ap.add_argument("--gemm", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
+                    help="time the tensor-core GEMM with the stochastic-rounding epilogue instead")
     args = ap.parse_args()
+    if args.gemm:
+        return run_gemm(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

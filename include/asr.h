@@ -186,6 +186,25 @@ asr_status asr_adamw_sr_multi_tensor(const asr_tensor_desc *table, int32_t n_ten
 asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_t n_tensors,
                                             const asr_adamw_hparams *hp, asr_stream_t stream);
 
+/* bf16 GEMM with a stochastic-rounding epilogue on the tensor cores ("Add
+ * stochastic rounding and philox RNG helpers", Consumer: the bf16 GEMM's
+ * f32 accumulator converts to bf16 by stochastic rounding, keyed per output
+ * element from a seed, instead of round-to-nearest).
+ * C = A . B^T with A: m x k, B: n x k, C: m x n, all row-major bf16 patterns
+ * (device, caller-owned); f32 accumulation.  Output element (i, j) is
+ * rounded from its f32 accumulator acc(i, j) exactly as
+ * asr_stochastic_round_bf16 rounds element i*n + j with base_index 0 at
+ * (seed, step) (rounding = ASR_ROUND_SR), or to nearest-even
+ * (ASR_ROUND_RNE).  c_f32 (device, m x n f32, may be NULL) receives acc.
+ * Requirements: m a multiple of 128 (at most 128 * 65535), n a multiple of
+ * 128, k a multiple of 64, all pointers 16-byte aligned; otherwise
+ * ASR_ERR_INVALID_VALUE before any launch.  The summation order of acc is
+ * the tensor cores', so acc is reproducible run to run on one GPU model but
+ * not bitwise equal to a CPU sum. */
+asr_status asr_gemm_bf16_sr(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, uint64_t m,
+                            uint64_t n, uint64_t k, uint32_t rounding, uint32_t step, uint64_t seed,
+                            asr_stream_t stream);
+
 /* Static description of a status code. */
 const char *asr_status_string(asr_status status);
 

@@ -23,7 +23,7 @@ ASR_ROUND_SR, ASR_ROUND_RNE = 0, 1
 EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
            "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
            "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout",
-           "asr_adamw_sr_multi_tensor_static")
+           "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr")
 ASR_STATIC_TABLE_MAX = 4096
 
 
@@ -75,9 +75,11 @@ def lib() -> ctypes.CDLL:
                                                 ctypes.POINTER(AdamwHparams), vp]
         L.asr_adamw_sr_multi_tensor_static.argtypes = [ctypes.POINTER(TensorDesc), i32,
                                                        ctypes.POINTER(AdamwHparams), vp]
+        L.asr_gemm_bf16_sr.argtypes = [vp, vp, vp, vp, u64, u64, u64, u32, u32, u64, vp]
+        L.asr_gemm_bf16_sr.restype = ctypes.c_int
         for f in ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
                   "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor",
-                  "asr_adamw_sr_multi_tensor_static"):
+                  "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr"):
             getattr(L, f).restype = ctypes.c_int
         L.asr_status_string.argtypes = [ctypes.c_int]
         L.asr_status_string.restype = ctypes.c_char_p
@@ -284,4 +286,27 @@ def asr_adamw_sr_multi_tensor_static(tensors, *, lr, beta1=0.9, beta2=0.999, eps
     with torch.cuda.device(dev):
         _check(lib().asr_adamw_sr_multi_tensor_static(table, len(table), ctypes.byref(h),
                                                       _stream_handle(dev, stream)),
-               "asr_adamw_sr_multi_tensor_static")
+               "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr")
+
+
+def asr_gemm_bf16_sr(a, b, c, c_f32=None, *, rounding="sr", step=0, seed=0, stream=None):
+    """C = A . B^T on the tensor cores with a stochastic-rounding (or RNE)
+    bf16 epilogue.  a: (m, k), b: (n, k), c: (m, n) contiguous bfloat16 CUDA
+    tensors; c_f32: optional (m, n) float32 tensor receiving the accumulator."""
+    torch = _torch()
+    if a.dim() != 2 or b.dim() != 2 or c.dim() != 2:
+        raise ValueError("a, b and c must be 2-D")
+    m, k = a.shape
+    n = b.shape[0]
+    if b.shape[1] != k or tuple(c.shape) != (m, n):
+        raise ValueError(f"shapes do not chain: a {tuple(a.shape)}, b {tuple(b.shape)}, c {tuple(c.shape)}")
+    pa = _dev_ptr(a, "a", (torch.bfloat16,))
+    pb = _dev_ptr(b, "b", (torch.bfloat16,))
+    pc = _dev_ptr(c, "c", (torch.bfloat16,))
+    pf = _dev_ptr(c_f32, "c_f32", (torch.float32,), m * n) if c_f32 is not None else None
+    r = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE}[rounding]
+    with torch.cuda.device(a.device):
+        _check(lib().asr_gemm_bf16_sr(pa, pb, pc, pf, m, n, k, r, int(step) & 0xFFFFFFFF,
+                                      int(seed) & (2**64 - 1), _stream_handle(a.device, stream)),
+               "asr_gemm_bf16_sr")
+    return c

@@ -13,6 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "csrc", "asr.cu")
 HDR = os.path.join(ROOT, "include", "asr.h")
+INCLUDED = [os.path.join(HERE, "csrc", "gemm_sr.cuh")]     # textually included by asr.cu
 LIB = os.path.join(HERE, "libasr.so")
 
 NVCC_FLAGS = [
@@ -32,7 +33,7 @@ def nvcc():
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the library if missing or older than its sources."""
-    deps = [SRC, HDR, __file__]
+    deps = [SRC, HDR, *INCLUDED, __file__]
     if (not force and os.path.exists(LIB)
             and all(os.path.getmtime(LIB) >= os.path.getmtime(d) for d in deps)):
         return LIB

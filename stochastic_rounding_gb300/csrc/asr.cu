@@ -22,6 +22,8 @@
 // elements, with the ten round keys precomputed on the host and read from the
 // constant bank.  Every float operation is an explicitly rounded IEEE binary32
 // intrinsic in a fixed order, so results are bit-reproducible.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -1411,6 +1413,8 @@ asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, con
     return ASR_OK;
 }
 
+#include "gemm_sr.cuh"
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -1545,6 +1549,12 @@ asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_
                                             const asr_adamw_hparams *hp, asr_stream_t stream)
 {
     return run_adamw_static(table, n_tensors, hp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+asr_status asr_gemm_bf16_sr(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, uint64_t m, uint64_t n,
+                            uint64_t k, uint32_t rounding, uint32_t step, uint64_t seed, asr_stream_t stream)
+{
+    return gemm::run(a, b, c, c_f32, m, n, k, rounding, step, seed, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,0 +1,317 @@
+// gemm_sr.cuh -- bf16 GEMM on the 5th-generation tensor cores with a
+// stochastic-rounding epilogue.  Included into asr.cu (inside its anonymous
+// namespace): it shares the Philox, rounding and mbarrier helpers and the
+// device error word with the optimizer kernels.
+//
+// "Add stochastic rounding and philox RNG helpers" (FlyDSL PR 907), section
+// Consumer: a bf16 GEMM gains a rounding option; with stochastic rounding the
+// f32 accumulator converts to bf16 through stochastic rounding, keyed per
+// output element from a seed, instead of round-to-nearest.  Here output
+// element (i, j) of the M x N result has global index i*N + j and draws its
+// random bits exactly as every other element of this library does: word
+// (e & 3) of Philox4x32-10 at counter ((e>>2) lo, (e>>2) hi, step, 0) under
+// key (seed lo, seed hi).  So the GEMM's output is
+// asr_stochastic_round_bf16(acc, base 0, step, seed) of its own f32
+// accumulator acc.
+//
+// C[M,N] = A[M,K] . B[N,K]^T, all row-major (both operands K-contiguous, as
+// nn.Linear keeps its weight).  One CTA computes one 128 x 128 tile:
+//   warp 0, lane 0   streams 128 x 64 slices of A and B into a ring of
+//                    shared-memory stages (tensor-map bulk copies, 128-byte
+//                    swizzle), completion counted on a per-stage mbarrier;
+//   warp 1           owns the tensor memory (allocates 128 columns = the
+//                    128 x 128 f32 accumulator, frees it at the end); its
+//                    lane 0 issues tcgen05.mma (kind::f16, bf16 in, f32
+//                    accumulate; four K=16 steps per slice) and commits each
+//                    slice to the stage's "empty" barrier and the last one to
+//                    the "accumulator ready" barrier;
+//   warps 2..5       read the accumulator rows of their TMEM lane quarter
+//                    with tcgen05.ld, round (stochastic or nearest-even),
+//                    and store bf16 (and, optionally, the f32 accumulator).
+// Every wait is bounded (mbar_wait); on a timeout the error bit is raised,
+// the thread skips ahead to the cleanup, and the tensor memory is still
+// freed.
+
+namespace gemm {
+
+constexpr int kBM = 128;                   // tile rows (M) = TMEM lanes
+constexpr int kBN = 128;                   // tile columns (N) = TMEM columns
+constexpr int kBK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 6;
+constexpr int kThreads = 192;              // 6 warps
+constexpr uint32_t kStageA = kBM * kBK * 2;     // 16 KB
+constexpr uint32_t kStageB = kBN * kBK * 2;     // 16 KB
+constexpr uint32_t kStageBytes = kStageA + kStageB;
+constexpr uint32_t kTmemCols = kBN;             // f32 accumulator columns
+// dynamic shared memory: 1 KB of alignment slack, the stages, 2*kStages+1
+// barriers and the TMEM address slot
+constexpr int kSmem = 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 16;
+
+// Instruction descriptor of tcgen05.mma kind::f16: f32 accumulator
+// (bits 4-5 = 1), A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both
+// K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kBN >> 3) << 17) |
+                                (uint32_t(kBM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major operand tile written by the
+// tensor map with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024
+// bytes apart (stride byte offset), leading byte offset unused (1), version
+// 1 (bits 46-47), layout "128-byte swizzle" (2, bits 61-63).  The start
+// address advances by 32 bytes per K=16 step inside the swizzle row.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct GemmParams {
+    uint16_t *c;            // M x N bf16
+    float *c_f32;           // M x N f32 accumulator copy, or null
+    uint32_t m, n, k;
+    uint32_t step;
+    uint32_t rounding;      // asr_rounding
+    RoundKeys keys;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ GemmParams P, uint64_t limit_ns)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;          // 1024-byte aligned for the 128-byte swizzle
+    const uint32_t bars = base + kStages * kStageBytes;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (kStages + s); };
+    const uint32_t acc_ready = bars + 8u * (2 * kStages);
+    const uint32_t tmem_slot = acc_ready + 8u;
+    const uint32_t *tmem_slot_ptr = reinterpret_cast<const uint32_t *>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+    const int kblocks = static_cast<int>(P.k / kBK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(acc_ready, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot_ptr;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------- producer
+        int issued = 0;
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t use = static_cast<uint32_t>(kb / kStages);
+            if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
+            mbar_arrive_expect_tx(full(s), kStageBytes);
+            const uint32_t dst = base + s * kStageBytes;
+            tma_load_2d(dst, &map_a, kb * kBK, static_cast<int32_t>(m0), full(s));
+            tma_load_2d(dst + kStageA, &map_b, kb * kBK, static_cast<int32_t>(n0), full(s));
+            ++issued;
+        }
+        // the copies issued here must land before the CTA exits
+        for (int s = 0; s < kStages && s < issued; ++s) {
+            const uint32_t last_use = static_cast<uint32_t>((issued - 1 - s) / kStages);
+            mbar_wait(full(s), last_use & 1u, limit_ns);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------ MMA issuer
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t use = static_cast<uint32_t>(kb / kStages);
+            if (!mbar_wait(full(s), use & 1u, limit_ns)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t a = base + s * kStageBytes, b = a + kStageA;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_bf16(tmem, smem_desc(a + kk * 32), smem_desc(b + kk * 32), (kb | kk) != 0);
+            mma_commit(empty(s));               // the stage is free once these MMAs have read it
+        }
+        mma_commit(acc_ready);                  // fires when every MMA above has completed
+    } else if (warp >= 2) {
+        // ------------------------------------------------------- epilogue
+        // tcgen05.ld is warp-collective: the warp agrees on readiness (and
+        // reconverges) first; on a timeout it reads and stores nothing
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_ready, 0, limit_ns));
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const int quarter = warp & 3;                       // TMEM lanes this warp may read
+        const uint32_t row = m0 + quarter * 32 + lane;
+        const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        for (int c = 0; ok && c < kBN; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tq + c, v);
+            const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
+            uint32_t w[8];
+            if (P.rounding == ASR_ROUND_SR) {
+                uint32_t r[16];
+                philox_q(e0 >> 2, P.step, P.keys, r);
+                philox_q((e0 >> 2) + 1, P.step, P.keys, r + 4);
+                philox_q((e0 >> 2) + 2, P.step, P.keys, r + 8);
+                philox_q((e0 >> 2) + 3, P.step, P.keys, r + 12);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    w[k] = sr_pack2<true>(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), r[2 * k],
+                                          r[2 * k + 1]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    w[k] = pack_bf16(round_rne(__uint_as_float(v[2 * k])), round_rne(__uint_as_float(v[2 * k + 1])));
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            if (P.c_f32) {
+                uint4 *df = reinterpret_cast<uint4 *>(P.c_f32 + e0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) df[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+    }
+    // ------------------------------------------------------------ cleanup
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// Tensor-map encoder from the driver, fetched through the runtime (the
+// library does not link libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+asr_status encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
+{
+    std::lock_guard<std::mutex> lk(g_encode_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(cudaErrorNotSupported);
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return ASR_OK;
+}
+
+// The kernel's dynamic shared memory is above the default 48 KB: opt in once
+// per device.
+bool g_smem_opted[kMaxDevices];
+
+asr_status smem_opt_in()
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ASR_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lk(g_encode_mu);
+    if (!g_smem_opted[dev]) {
+        e = cudaFuncSetAttribute(gemm_bf16_sr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_smem_opted[dev] = true;
+    }
+    return ASR_OK;
+}
+
+// Row-major rows x k bf16 matrix, boxes of box_rows x 64 with 128-byte swizzle.
+asr_status make_map(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t k, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    asr_status st = encoder(&enc);
+    if (st != ASR_OK) return st;
+    const cuuint64_t dims[2] = {k, rows};
+    const cuuint64_t strides[1] = {k * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ASR_OK : ASR_ERR_INVALID_VALUE;
+}
+
+asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, uint64_t m, uint64_t n,
+               uint64_t k, uint32_t rounding, uint32_t step, uint64_t seed, cudaStream_t stream)
+{
+    if (rounding != ASR_ROUND_SR && rounding != ASR_ROUND_RNE) return ASR_ERR_UNSUPPORTED_DTYPE;
+    if (m == 0 || n == 0) return ASR_OK;
+    if (!a || !b || !c) return ASR_ERR_INVALID_VALUE;
+    if (m % kBM || n % kBN || k == 0 || k % kBK) return ASR_ERR_INVALID_VALUE;
+    if (m / kBM > 65535 || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
+        return ASR_ERR_INVALID_VALUE;
+    CUtensorMap ma, mb;
+    asr_status st = make_map(&ma, a, m, k, kBM);
+    if (st != ASR_OK) return st;
+    st = make_map(&mb, b, n, k, kBN);
+    if (st != ASR_OK) return st;
+    st = smem_opt_in();
+    if (st != ASR_OK) return st;
+    GemmParams P;
+    P.c = c;
+    P.c_f32 = c_f32;
+    P.m = static_cast<uint32_t>(m);
+    P.n = static_cast<uint32_t>(n);
+    P.k = static_cast<uint32_t>(k);
+    P.step = step;
+    P.rounding = rounding;
+    P.keys = make_keys(seed);
+    const dim3 grid(static_cast<unsigned>(n / kBN), static_cast<unsigned>(m / kBM));
+    gemm_bf16_sr_kernel<<<grid, kThreads, kSmem, stream>>>(ma, mb, P, kWaitLimitNs);
+    return check_launch();
+}
+
+}  // namespace gemm

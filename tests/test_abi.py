@@ -148,3 +148,16 @@ def test_oracle_is_not_imported_by_the_product():
                     text = f.read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "asr_oracle" not in text, fn
+
+
+def test_gemm_rejects_bad_shapes_before_launching(L):
+    """Shape, pointer and alignment checks of the GEMM run before any CUDA
+    call (no GPU needed)."""
+    p = ctypes.c_void_p(4096)
+    g = L.asr_gemm_bf16_sr
+    for m, n, k in ((100, 128, 64), (128, 100, 64), (128, 128, 48), (128, 128, 0), (128 * 65536, 128, 64)):
+        assert g(p, p, p, None, m, n, k, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE, (m, n, k)
+    assert g(None, p, p, None, 128, 128, 64, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE
+    assert g(ctypes.c_void_p(4097), p, p, None, 128, 128, 64, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE
+    assert g(p, p, p, None, 128, 128, 64, 7, 1, 0, None) == _lib.ASR_ERR_UNSUPPORTED_DTYPE
+    assert g(None, None, None, None, 0, 128, 64, 0, 1, 0, None) == _lib.ASR_OK

@@ -1,0 +1,120 @@
+"""GPU parity of the tcgen05 bf16 GEMM with a stochastic-rounding epilogue
+("Add stochastic rounding and philox RNG helpers", Consumer).
+
+The tensor cores' summation order is not a CPU's, so the f32 accumulator is
+checked against a binary64 product within the error bound of an f32 sum of K
+products; the bf16 output is then checked bit for bit against the oracle's
+rounding of that very accumulator (element (i, j) at global index i*N + j),
+which pins the epilogue exactly."""
+import numpy as np
+import pytest
+
+from gpu_util import assert_same_bits, host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def asr():
+    torch_cuda()
+    from stochastic_rounding_gb300 import build
+    build.build()
+    import stochastic_rounding_gb300 as m
+    m.lib()
+    return m
+
+
+def _operands(m, n, k, seed, scale=1.0):
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    a = (torch.randn(m, k, device="cuda", generator=g) * scale).to(torch.bfloat16)
+    b = (torch.randn(n, k, device="cuda", generator=g) * scale).to(torch.bfloat16)
+    return a, b
+
+
+def _check_accumulator(a, b, acc):
+    """|acc - A.B^T| <= 2 K u sum_k |a_ik b_jk| with u = 2^-24 (an f32 sum of
+    K exact products, allowing the tensor cores' own rounding)."""
+    import torch
+    ad, bd = a.double(), b.double()
+    exact = ad @ bd.t()
+    mag = ad.abs() @ bd.abs().t()
+    k = a.shape[1]
+    err = (acc.double() - exact).abs()
+    bound = 2 * k * 2.0 ** -24 * mag + 1e-30
+    worst = float((err / bound).max())
+    assert worst <= 1.0, f"accumulator off the binary64 product by {worst:.3g} x the bound"
+
+
+@pytest.mark.parametrize("m,n,k", [(128, 128, 64), (256, 384, 512), (128, 256, 64 * 13)])
+@pytest.mark.parametrize("rounding", ["sr", "rne"])
+def test_gemm_matches_oracle_rounding_of_accumulator(asr, orc, m, n, k, rounding):
+    import torch
+    a, b = _operands(m, n, k, seed=m + n + k)
+    c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, rounding=rounding, step=3, seed=2**40 + 9)
+    torch.cuda.synchronize()
+    _check_accumulator(a, b, acc)
+    acc_h = host(acc).reshape(-1)
+    want = orc.sr_fill(acc_h, 0, 3, 2**40 + 9) if rounding == "sr" else orc.rne_fill(acc_h)
+    assert_same_bits(host(c).reshape(-1), want, f"gemm {m}x{n}x{k} {rounding}", nan_equal=False)
+
+
+def test_gemm_large_equals_standalone_rounding(asr, orc):
+    """2048 x 2048 x 4096: the epilogue equals the library's stand-alone
+    rounding op (itself bit-exact with the oracle) on the accumulator, the
+    accumulator is within the bound, and sampled rows match the oracle."""
+    import torch
+    m, n, k = 2048, 2048, 4096
+    a, b = _operands(m, n, k, seed=7, scale=0.5)
+    c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, step=11, seed=5)
+    ref = torch.empty(m * n, dtype=torch.int16, device="cuda")
+    asr.asr_stochastic_round_bf16(acc.view(-1), ref, base_index=0, step=11, seed=5)
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16).view(-1), ref)
+    _check_accumulator(a, b, acc)
+    rng = np.random.default_rng(3)
+    for i in rng.integers(0, m, 8):
+        row = host(acc[int(i)])
+        want = orc.sr_fill(row, int(i) * n, 11, 5)
+        assert_same_bits(host(c[int(i)]), want, f"row {int(i)}", nan_equal=False)
+    assert asr.asr_take_device_error() == 0
+
+
+def test_gemm_seed_keying_and_unbiasedness(asr):
+    """Same (seed, step) -> identical output; a new seed changes it; over 64
+    seeds the mean of the bf16 outputs approaches the accumulator."""
+    import torch
+    m, n, k = 256, 256, 256
+    a, b = _operands(m, n, k, seed=1)
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    outs = []
+    for seed in range(64):
+        c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        asr.asr_gemm_bf16_sr(a, b, c, acc if seed == 0 else None, step=1, seed=seed)
+        outs.append(c.float())
+    c0 = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c0, None, step=1, seed=0)
+    torch.cuda.synchronize()
+    assert torch.equal(c0.float(), outs[0])
+    assert not torch.equal(outs[0], outs[1])
+    mean = torch.stack(outs).mean(0)
+    rn = acc.to(torch.bfloat16).float()
+    # the SR mean is far closer to the accumulator than round-to-nearest is
+    assert float((mean - acc).abs().mean()) < 0.25 * float((rn - acc).abs().mean())
+
+
+def test_gemm_rejects_unsupported_shapes(asr):
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    a = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
+    L = _lib.lib()
+    for m, n, k in ((100, 128, 64), (128, 100, 64), (128, 128, 48)):
+        assert L.asr_gemm_bf16_sr(a.data_ptr(), b.data_ptr(), c.data_ptr(), None, m, n, k, 0, 1, 0, None) \
+            == _lib.ASR_ERR_INVALID_VALUE
