@@ -15,12 +15,14 @@
 // accumulator acc.
 //
 // C[M,N] = A[M,K] . B[N,K]^T, all row-major (both operands K-contiguous, as
-// nn.Linear keeps its weight).  One CTA computes one 128 x 128 tile:
-//   warp 0, lane 0   streams 128 x 64 slices of A and B into a ring of
+// nn.Linear keeps its weight).  One CTA computes one 128 x 256 tile (the
+// last one in N may be half outside, when N is an odd multiple of 128: the
+// tensor map reads zeros there and the epilogue stores only real columns):
+//   warp 0, lane 0   streams 128 x 64 and 256 x 64 slices of A and B into a ring of
 //                    shared-memory stages (tensor-map bulk copies, 128-byte
 //                    swizzle), completion counted on a per-stage mbarrier;
-//   warp 1           owns the tensor memory (allocates 128 columns = the
-//                    128 x 128 f32 accumulator, frees it at the end); its
+//   warp 1           owns the tensor memory (allocates 256 columns = the
+//                    128 x 256 f32 accumulator, frees it at the end); its
 //                    lane 0 issues tcgen05.mma (kind::f16, bf16 in, f32
 //                    accumulate; four K=16 steps per slice) and commits each
 //                    slice to the stage's "empty" barrier and the last one to
@@ -35,12 +37,12 @@
 namespace gemm {
 
 constexpr int kBM = 128;                   // tile rows (M) = TMEM lanes
-constexpr int kBN = 128;                   // tile columns (N) = TMEM columns
+constexpr int kBN = 256;                   // tile columns (N) = TMEM columns
 constexpr int kBK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kThreads = 192;              // 6 warps
 constexpr uint32_t kStageA = kBM * kBK * 2;     // 16 KB
-constexpr uint32_t kStageB = kBN * kBK * 2;     // 16 KB
+constexpr uint32_t kStageB = kBN * kBK * 2;     // 32 KB
 constexpr uint32_t kStageBytes = kStageA + kStageB;
 constexpr uint32_t kTmemCols = kBN;             // f32 accumulator columns
 // dynamic shared memory: 1 KB of alignment slack, the stages, 2*kStages+1
@@ -187,7 +189,8 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         const int quarter = warp & 3;                       // TMEM lanes this warp may read
         const uint32_t row = m0 + quarter * 32 + lane;
         const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        for (int c = 0; ok && c < kBN; c += 16) {
+        const int ncols = static_cast<int>(P.n - n0) < kBN ? static_cast<int>(P.n - n0) : kBN;
+        for (int c = 0; ok && c < ncols; c += 16) {
             uint32_t v[16];
             tmem_ld16(tq + c, v);
             const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
@@ -289,7 +292,7 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (rounding != ASR_ROUND_SR && rounding != ASR_ROUND_RNE) return ASR_ERR_UNSUPPORTED_DTYPE;
     if (m == 0 || n == 0) return ASR_OK;
     if (!a || !b || !c) return ASR_ERR_INVALID_VALUE;
-    if (m % kBM || n % kBN || k == 0 || k % kBK) return ASR_ERR_INVALID_VALUE;
+    if (m % kBM || n % 128 || k == 0 || k % kBK) return ASR_ERR_INVALID_VALUE;
     if (m / kBM > 65535 || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
         return ASR_ERR_INVALID_VALUE;
@@ -309,7 +312,7 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     P.step = step;
     P.rounding = rounding;
     P.keys = make_keys(seed);
-    const dim3 grid(static_cast<unsigned>(n / kBN), static_cast<unsigned>(m / kBM));
+    const dim3 grid(static_cast<unsigned>((n + kBN - 1) / kBN), static_cast<unsigned>(m / kBM));
     gemm_bf16_sr_kernel<<<grid, kThreads, kSmem, stream>>>(ma, mb, P, kWaitLimitNs);
     return check_launch();
 }
