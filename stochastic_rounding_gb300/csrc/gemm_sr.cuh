@@ -15,21 +15,26 @@
 // accumulator acc.
 //
 // C[M,N] = A[M,K] . B[N,K]^T, all row-major (both operands K-contiguous, as
-// nn.Linear keeps its weight).  One CTA computes one 128 x 256 tile (the
-// last one in N may be half outside, when N is an odd multiple of 128: the
-// tensor map reads zeros there and the epilogue stores only real columns):
-//   warp 0, lane 0   streams 128 x 64 and 256 x 64 slices of A and B into a ring of
-//                    shared-memory stages (tensor-map bulk copies, 128-byte
-//                    swizzle), completion counted on a per-stage mbarrier;
-//   warp 1           owns the tensor memory (allocates 256 columns = the
-//                    128 x 256 f32 accumulator, frees it at the end); its
-//                    lane 0 issues tcgen05.mma (kind::f16, bf16 in, f32
-//                    accumulate; four K=16 steps per slice) and commits each
-//                    slice to the stage's "empty" barrier and the last one to
-//                    the "accumulator ready" barrier;
+// nn.Linear keeps its weight), in 128 x 256 tiles (the last one in N may be
+// half outside when N is an odd multiple of 128: the tensor map reads zeros
+// there and the epilogue stores only real columns).  Persistent: one CTA per
+// SM walks the tiles in a grouped order (16 M-tiles at a time across N, so
+// the tiles in flight share operands in L2):
+//   warp 0, lane 0   streams 128 x 64 and 256 x 64 slices of A and B into a
+//                    4-stage shared-memory ring (tensor-map bulk copies,
+//                    128-byte swizzle), completion counted on mbarriers;
+//   warp 1           owns the tensor memory: all 512 columns, two 128 x 256
+//                    f32 accumulators; its lane 0 issues tcgen05.mma
+//                    (kind::f16, bf16 in, f32 accumulate; four K=16 steps
+//                    per slice), commits each slice to its stage's "empty"
+//                    barrier and each tile to its accumulator's "full"
+//                    barrier, and waits for the epilogue to hand an
+//                    accumulator back before reusing it;
 //   warps 2..5       read the accumulator rows of their TMEM lane quarter
 //                    with tcgen05.ld, round (stochastic or nearest-even),
-//                    and store bf16 (and, optionally, the f32 accumulator).
+//                    store bf16 (and, optionally, the f32 accumulator) and
+//                    release the accumulator -- while the next tile's
+//                    products already go into the other one.
 // Every wait is bounded (mbar_wait); on a timeout the error bit is raised,
 // the thread skips ahead to the cleanup, and the tensor memory is still
 // freed.
@@ -41,13 +46,17 @@ constexpr int kBN = 256;                   // tile columns (N) = TMEM columns
 constexpr int kBK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kThreads = 192;              // 6 warps
+constexpr int kEpilogueWarps = 4;
+constexpr int kGroupM = 16;                // tile order: 16 M-tiles walked across N, group by group
 constexpr uint32_t kStageA = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kStageB = kBN * kBK * 2;     // 32 KB
 constexpr uint32_t kStageBytes = kStageA + kStageB;
-constexpr uint32_t kTmemCols = kBN;             // f32 accumulator columns
-// dynamic shared memory: 1 KB of alignment slack, the stages, 2*kStages+1
-// barriers and the TMEM address slot
-constexpr int kSmem = 1024 + kStages * kStageBytes + (2 * kStages + 1) * 8 + 16;
+constexpr int kAccBufs = 2;                     // two accumulators: the epilogue of one tile
+                                                // overlaps the main loop of the next
+constexpr uint32_t kTmemCols = kBN * kAccBufs;  // 512 f32 columns = all of the tensor memory
+// dynamic shared memory: 1 KB of alignment slack, the stages, the barriers
+// (full/empty per stage, full/empty per accumulator) and the TMEM address slot
+constexpr int kSmem = 1024 + kStages * kStageBytes + (2 * kStages + 2 * kAccBufs) * 8 + 16;
 
 // Instruction descriptor of tcgen05.mma kind::f16: f32 accumulator
 // (bits 4-5 = 1), A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both
@@ -111,6 +120,20 @@ struct GemmParams {
     RoundKeys keys;
 };
 
+// Tile t of the grouped order: groups of kGroupM M-tiles, walked column by
+// column across N (M fastest inside a group).
+__device__ __forceinline__ void tile_coords(uint32_t t, uint32_t tiles_m, uint32_t tiles_n, uint32_t &mt,
+                                            uint32_t &nt)
+{
+    const uint32_t group_size = kGroupM * tiles_n;
+    const uint32_t first_m = (t / group_size) * kGroupM;
+    const uint32_t gm = tiles_m - first_m < static_cast<uint32_t>(kGroupM) ? tiles_m - first_m : kGroupM;
+    const uint32_t local = t % group_size;
+    mt = first_m + local % gm;
+    nt = local / gm;
+}
+
+// Persistent: each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ...
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const __grid_constant__ GemmParams P, uint64_t limit_ns)
@@ -121,12 +144,14 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     const uint32_t bars = base + kStages * kStageBytes;
     auto full = [&](int s) { return bars + 8u * s; };
     auto empty = [&](int s) { return bars + 8u * (kStages + s); };
-    const uint32_t acc_ready = bars + 8u * (2 * kStages);
-    const uint32_t tmem_slot = acc_ready + 8u;
+    auto acc_full = [&](int b) { return bars + 8u * (2 * kStages + b); };
+    auto acc_empty = [&](int b) { return bars + 8u * (2 * kStages + kAccBufs + b); };
+    const uint32_t tmem_slot = bars + 8u * (2 * kStages + 2 * kAccBufs);
     const uint32_t *tmem_slot_ptr = reinterpret_cast<const uint32_t *>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+    const uint32_t tiles_m = P.m / kBM, tiles_n = (P.n + kBN - 1) / kBN;
+    const uint32_t tiles = tiles_m * tiles_n;
     const int kblocks = static_cast<int>(P.k / kBK);
 
     if (threadIdx.x == 0) {
@@ -134,7 +159,10 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(acc_ready, 1);
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), kEpilogueWarps);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -150,74 +178,107 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------- producer
-        int issued = 0;
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t use = static_cast<uint32_t>(kb / kStages);
-            if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
-            mbar_arrive_expect_tx(full(s), kStageBytes);
-            const uint32_t dst = base + s * kStageBytes;
-            tma_load_2d(dst, &map_a, kb * kBK, static_cast<int32_t>(m0), full(s));
-            tma_load_2d(dst + kStageA, &map_b, kb * kBK, static_cast<int32_t>(n0), full(s));
-            ++issued;
+        uint32_t g = 0;                          // slices issued, over all tiles
+        bool ok = true;
+        for (uint32_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            uint32_t mt, nt;
+            tile_coords(t, tiles_m, tiles_n, mt, nt);
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                const int s = static_cast<int>(g % kStages);
+                const uint32_t use = g / kStages;
+                if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full(s), kStageBytes);
+                const uint32_t dst = base + s * kStageBytes;
+                tma_load_2d(dst, &map_a, kb * kBK, static_cast<int32_t>(mt * kBM), full(s));
+                tma_load_2d(dst + kStageA, &map_b, kb * kBK, static_cast<int32_t>(nt * kBN), full(s));
+            }
         }
         // the copies issued here must land before the CTA exits
-        for (int s = 0; s < kStages && s < issued; ++s) {
-            const uint32_t last_use = static_cast<uint32_t>((issued - 1 - s) / kStages);
-            mbar_wait(full(s), last_use & 1u, limit_ns);
+        for (uint32_t s = 0; s < static_cast<uint32_t>(kStages) && s < g; ++s) {
+            const uint32_t last_use = (g - 1 - s) / kStages;
+            mbar_wait(full(static_cast<int>(s)), last_use & 1u, limit_ns);
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t use = static_cast<uint32_t>(kb / kStages);
-            if (!mbar_wait(full(s), use & 1u, limit_ns)) break;
+        uint32_t g = 0, i = 0;
+        bool ok = true;
+        for (uint32_t t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++i) {
+            const int b = static_cast<int>(i % kAccBufs);
+            const uint32_t ub = i / kAccBufs;
+            if (ub > 0 && !mbar_wait(acc_empty(b), (ub - 1) & 1u, limit_ns)) break;   // epilogue done with b
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t a = base + s * kStageBytes, b = a + kStageA;
+            const uint32_t d = tmem + static_cast<uint32_t>(b * kBN);
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                const int s = static_cast<int>(g % kStages);
+                const uint32_t use = g / kStages;
+                if (!mbar_wait(full(s), use & 1u, limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t sa = base + s * kStageBytes, sb = sa + kStageA;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-                mma_bf16(tmem, smem_desc(a + kk * 32), smem_desc(b + kk * 32), (kb | kk) != 0);
-            mma_commit(empty(s));               // the stage is free once these MMAs have read it
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_bf16(d, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), (kb | kk) != 0);
+                mma_commit(empty(s));           // the stage is free once these MMAs have read it
+            }
+            mma_commit(acc_full(b));            // fires when every MMA of this tile has completed
         }
-        mma_commit(acc_ready);                  // fires when every MMA above has completed
     } else if (warp >= 2) {
         // ------------------------------------------------------- epilogue
-        // tcgen05.ld is warp-collective: the warp agrees on readiness (and
-        // reconverges) first; on a timeout it reads and stores nothing
-        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_ready, 0, limit_ns));
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const int quarter = warp & 3;                       // TMEM lanes this warp may read
-        const uint32_t row = m0 + quarter * 32 + lane;
-        const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int ncols = static_cast<int>(P.n - n0) < kBN ? static_cast<int>(P.n - n0) : kBN;
-        for (int c = 0; ok && c < ncols; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(tq + c, v);
-            const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
-            uint32_t w[8];
-            if (P.rounding == ASR_ROUND_SR) {
-                uint32_t r[16];
-                philox_q(e0 >> 2, P.step, P.keys, r);
-                philox_q((e0 >> 2) + 1, P.step, P.keys, r + 4);
-                philox_q((e0 >> 2) + 2, P.step, P.keys, r + 8);
-                philox_q((e0 >> 2) + 3, P.step, P.keys, r + 12);
+        uint32_t i = 0;
+        for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+            const int b = static_cast<int>(i % kAccBufs);
+            const uint32_t ub = i / kAccBufs;
+            // tcgen05.ld is warp-collective: the warp agrees on readiness (and
+            // reconverges) first; on a timeout it stops
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(b), ub & 1u, limit_ns))) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            uint32_t mt, nt;
+            tile_coords(t, tiles_m, tiles_n, mt, nt);
+            const uint32_t row = mt * kBM + quarter * 32 + lane;
+            const uint32_t n0 = nt * kBN;
+            const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * kBN);
+            const int ncols = static_cast<int>(P.n - n0) < kBN ? static_cast<int>(P.n - n0) : kBN;
+            for (int c = 0; c < ncols; c += 16) {
+                uint32_t v[16];
+                tmem_ld16(tq + c, v);
+                const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
+                uint32_t w[8];
+                if (P.rounding == ASR_ROUND_SR) {
+                    uint32_t r[16];
+                    philox_q(e0 >> 2, P.step, P.keys, r);
+                    philox_q((e0 >> 2) + 1, P.step, P.keys, r + 4);
+                    philox_q((e0 >> 2) + 2, P.step, P.keys, r + 8);
+                    philox_q((e0 >> 2) + 3, P.step, P.keys, r + 12);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    w[k] = sr_pack2<true>(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), r[2 * k],
-                                          r[2 * k + 1]);
-            } else {
+                    for (int k = 0; k < 8; ++k)
+                        w[k] = sr_pack2<true>(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), r[2 * k],
+                                              r[2 * k + 1]);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    w[k] = pack_bf16(round_rne(__uint_as_float(v[2 * k])), round_rne(__uint_as_float(v[2 * k + 1])));
+                    for (int k = 0; k < 8; ++k)
+                        w[k] = pack_bf16(round_rne(__uint_as_float(v[2 * k])),
+                                         round_rne(__uint_as_float(v[2 * k + 1])));
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                if (P.c_f32) {
+                    uint4 *df = reinterpret_cast<uint4 *>(P.c_f32 + e0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        df[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            if (P.c_f32) {
-                uint4 *df = reinterpret_cast<uint4 *>(P.c_f32 + e0);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) df[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+            // this warp is done reading accumulator b
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(b));
         }
     }
     // ------------------------------------------------------------ cleanup
@@ -312,7 +373,12 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     P.step = step;
     P.rounding = rounding;
     P.keys = make_keys(seed);
-    const dim3 grid(static_cast<unsigned>((n + kBN - 1) / kBN), static_cast<unsigned>(m / kBM));
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const uint64_t tiles = (m / kBM) * ((n + kBN - 1) / kBN);
+    const unsigned grid = static_cast<unsigned>(tiles < static_cast<uint64_t>(sms) ? tiles : sms);
     gemm_bf16_sr_kernel<<<grid, kThreads, kSmem, stream>>>(ma, mb, P, kWaitLimitNs);
     return check_launch();
 }

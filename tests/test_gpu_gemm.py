@@ -118,3 +118,26 @@ def test_gemm_rejects_unsupported_shapes(asr):
     for m, n, k in ((100, 128, 64), (128, 100, 64), (128, 128, 48)):
         assert L.asr_gemm_bf16_sr(a.data_ptr(), b.data_ptr(), c.data_ptr(), None, m, n, k, 0, 1, 0, None) \
             == _lib.ASR_ERR_INVALID_VALUE
+
+
+def test_gemm_many_tiles_per_cta(asr, orc):
+    """4096 x 4224 x 256: 544 tiles (half tiles at the N edge) on 152 SMs, so
+    every CTA reuses both accumulators several times; the epilogue equals the
+    stand-alone rounding of the accumulator, which is within the bound, and
+    sampled rows match the oracle."""
+    import torch
+    m, n, k = 4096, 4224, 256
+    a, b = _operands(m, n, k, seed=12)
+    c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, step=2, seed=77)
+    ref = torch.empty(m * n, dtype=torch.int16, device="cuda")
+    asr.asr_stochastic_round_bf16(acc.view(-1), ref, base_index=0, step=2, seed=77)
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16).view(-1), ref)
+    _check_accumulator(a, b, acc)
+    rng = np.random.default_rng(4)
+    for i in rng.integers(0, m, 6):
+        want = orc.sr_fill(host(acc[int(i)]), int(i) * n, 2, 77)
+        assert_same_bits(host(c[int(i)]), want, f"row {int(i)}", nan_equal=False)
+    assert asr.asr_take_device_error() == 0
