@@ -196,9 +196,9 @@ asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_
  * asr_stochastic_round_bf16 rounds element i*n + j with base_index 0 at
  * (seed, step) (rounding = ASR_ROUND_SR), or to nearest-even
  * (ASR_ROUND_RNE).  c_f32 (device, m x n f32, may be NULL) receives acc.
- * Requirements: m a multiple of 128 (at most 128 * 65535), n a multiple of
- * 128, k a multiple of 64, all pointers 16-byte aligned; otherwise
- * ASR_ERR_INVALID_VALUE before any launch.  The summation order of acc is
+ * Requirements: n a multiple of 16, k a multiple of 8 (and k >= 8), m, n, k
+ * at most 2^24, all pointers 16-byte aligned; otherwise
+ * ASR_ERR_INVALID_VALUE before any launch.  m == 0 or n == 0 is a no-op.  The summation order of acc is
  * the tensor cores', so acc is reproducible run to run on one GPU model but
  * not bitwise equal to a CPU sum. */
 asr_status asr_gemm_bf16_sr(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, uint64_t m,

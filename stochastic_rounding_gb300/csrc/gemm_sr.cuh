@@ -15,9 +15,9 @@
 // accumulator acc.
 //
 // C[M,N] = A[M,K] . B[N,K]^T, all row-major (both operands K-contiguous, as
-// nn.Linear keeps its weight), in 128 x 256 tiles (the last one in N may be
-// half outside when N is an odd multiple of 128: the tensor map reads zeros
-// there and the epilogue stores only real columns).  Persistent: one CTA per
+// nn.Linear keeps its weight), in 128 x 256 tiles.  Edges: the tensor maps
+// read zeros past M, N and K (zeros add nothing to the sums), and the
+// epilogue stores only rows < M and columns < N.  Persistent: one CTA per
 // SM walks the tiles in a grouped order (16 M-tiles at a time across N, so
 // the tiles in flight share operands in L2):
 //   warp 0, lane 0   streams 128 x 64 and 256 x 64 slices of A and B into a
@@ -150,9 +150,9 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
     const uint32_t *tmem_slot_ptr = reinterpret_cast<const uint32_t *>(smem_raw + (tmem_slot - raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tiles_m = P.m / kBM, tiles_n = (P.n + kBN - 1) / kBN;
+    const uint32_t tiles_m = (P.m + kBM - 1) / kBM, tiles_n = (P.n + kBN - 1) / kBN;
     const uint32_t tiles = tiles_m * tiles_n;
-    const int kblocks = static_cast<int>(P.k / kBK);
+    const int kblocks = static_cast<int>((P.k + kBK - 1) / kBK);     // a short last slice reads zeros past K
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -246,7 +246,8 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             const int ncols = static_cast<int>(P.n - n0) < kBN ? static_cast<int>(P.n - n0) : kBN;
             for (int c = 0; c < ncols; c += 16) {
                 uint32_t v[16];
-                tmem_ld16(tq + c, v);
+                tmem_ld16(tq + c, v);               // warp-collective: every lane loads
+                if (row >= P.m) continue;           // rows past M (zeros read past the edge) are not stored
                 const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
                 uint32_t w[8];
                 if (P.rounding == ASR_ROUND_SR) {
@@ -353,8 +354,8 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (rounding != ASR_ROUND_SR && rounding != ASR_ROUND_RNE) return ASR_ERR_UNSUPPORTED_DTYPE;
     if (m == 0 || n == 0) return ASR_OK;
     if (!a || !b || !c) return ASR_ERR_INVALID_VALUE;
-    if (m % kBM || n % 128 || k == 0 || k % kBK) return ASR_ERR_INVALID_VALUE;
-    if (m / kBM > 65535 || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
+    if (n % 16 || k == 0 || k % 8) return ASR_ERR_INVALID_VALUE;
+    if (m > (1u << 24) || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
         return ASR_ERR_INVALID_VALUE;
     CUtensorMap ma, mb;
@@ -377,7 +378,8 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    const uint64_t tiles = (m / kBM) * ((n + kBN - 1) / kBN);
+    const uint64_t tiles = ((m + kBM - 1) / kBM) * ((n + kBN - 1) / kBN);
+    if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
     const unsigned grid = static_cast<unsigned>(tiles < static_cast<uint64_t>(sms) ? tiles : sms);
     gemm_bf16_sr_kernel<<<grid, kThreads, kSmem, stream>>>(ma, mb, P, kWaitLimitNs);
     return check_launch();

@@ -47,7 +47,8 @@ def _check_accumulator(a, b, acc):
     assert worst <= 1.0, f"accumulator off the binary64 product by {worst:.3g} x the bound"
 
 
-@pytest.mark.parametrize("m,n,k", [(128, 128, 64), (256, 384, 512), (128, 256, 64 * 13)])
+@pytest.mark.parametrize("m,n,k", [(128, 128, 64), (256, 384, 512), (128, 256, 64 * 13), (1, 16, 8),
+                                   (200, 272, 520), (333, 1040, 72)])
 @pytest.mark.parametrize("rounding", ["sr", "rne"])
 def test_gemm_matches_oracle_rounding_of_accumulator(asr, orc, m, n, k, rounding):
     import torch
@@ -115,7 +116,7 @@ def test_gemm_rejects_unsupported_shapes(asr):
     b = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
     c = torch.zeros(128, 128, dtype=torch.bfloat16, device="cuda")
     L = _lib.lib()
-    for m, n, k in ((100, 128, 64), (128, 100, 64), (128, 128, 48)):
+    for m, n, k in ((128, 100, 64), (128, 128, 60), (128, 128, 0)):
         assert L.asr_gemm_bf16_sr(a.data_ptr(), b.data_ptr(), c.data_ptr(), None, m, n, k, 0, 1, 0, None) \
             == _lib.ASR_ERR_INVALID_VALUE
 
