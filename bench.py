@@ -193,6 +193,49 @@ def e2e_chunks(tensors, offset, max_params=1 << 28):
     return res
 
 
+def _oracle_shard_worker(args):
+    """One process of the all-cores oracle run: its own window of the 8B
+    layout, one step, timed inside the process."""
+    shard, per, seed = args
+    import numpy as np
+
+    import oracle
+    from stochastic_rounding_gb300 import workloads as W
+    o = oracle.get()
+    table = W.param_table(W.LLAMA_8B)
+    starts, _ = W.offsets(table)
+    big = [i for i, (_, n, norm) in enumerate(table) if not norm]
+    t = big[shard % len(big)]
+    base = int(starts[t]) + (shard // len(big)) * per
+    hr = W.host_rng(seed, 100 + shard)
+    p = W.to_bf16_bits(W.normal_f32(hr, per, 0.02))
+    g = W.to_bf16_bits(W.normal_f32(hr, per, 1e-3))
+    m = np.zeros(per, np.float32)
+    v = np.zeros(per, np.float32)
+    t0 = time.perf_counter()
+    o.adamw_step(p, g, m, v, step=1, seed=0, base_index=base, **HP)
+    return per, time.perf_counter() - t0
+
+
+def start_oracle_pool():
+    """A spawn-started pool over the process's CPU affinity set (started
+    before the first GPU call, as forked children of a CUDA process hang)."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    return mp.get_context("spawn").Pool(cores), cores
+
+
+def cpu_oracle_all_cores(pool, cores, per=1 << 23):
+    """The same oracle, unchanged, one shard (a window of the 8B layout at its
+    true base index) per core, all cores at once: params/s over the wall time
+    of the slowest shard."""
+    results = pool.map(_oracle_shard_worker, [(i, per, 0) for i in range(cores)])
+    wall = max(dt for _, dt in results)
+    return {"value": sum(n for n, _ in results) / wall / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} processes x {per} params (one window of the 8B layout each), one step, "
+                      f"the oracle unchanged, sharded by base index"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -216,9 +259,12 @@ def run_reference(args):
 
 
 def run_gpu(args):
+    rank, world, local = dist_env()
+    pool = None
+    if rank == 0:
+        pool, pool_cores = start_oracle_pool()
     import torch
 
-    rank, world, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
@@ -300,40 +346,47 @@ def run_gpu(args):
     s_out = torch.cuda.Stream(device=dev)
     done_cmp = [None] * len(chunks)          # compute of chunk c finished (grads free)
     done_out = [None] * len(chunks)          # params of chunk c copied out (params free)
-    torch.cuda.synchronize(dev)
-    e_steps = max(1, args.steps)
     launches_e2e = 0
+
+    def e2e_steps(count):
+        nonlocal t_global, launches_e2e
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for _ in range(count):
+            t_global += 1
+            for c, (lo, hi, ctable) in enumerate(chunks):
+                ev_in = torch.cuda.Event()
+                with torch.cuda.stream(s_in):
+                    if done_cmp[c] is not None:
+                        s_in.wait_event(done_cmp[c])
+                    ps.g[lo:hi].copy_(g_host[lo:hi], non_blocking=True)
+                    ev_in.record(s_in)
+                stream.wait_event(ev_in)
+                if done_out[c] is not None:
+                    stream.wait_event(done_out[c])
+                asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
+                launches_e2e += 1
+                ev_c = torch.cuda.Event()
+                ev_c.record(stream)
+                done_cmp[c] = ev_c
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_c)
+                    p_host[lo:hi].copy_(ps.p[lo:hi], non_blocking=True)
+                    ev_o = torch.cuda.Event()
+                    ev_o.record(s_out)
+                done_out[c] = ev_o
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    e2e_steps(args.warmup)                   # untimed, like the device-resident leg
+    torch.cuda.synchronize(dev)
+    launches_e2e = 0
+    e_steps = max(1, args.steps)
     barrier()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    s_in.wait_stream(stream)
-    s_out.wait_stream(stream)
-    for _ in range(e_steps):
-        t_global += 1
-        for c, (lo, hi, ctable) in enumerate(chunks):
-            ev_in = torch.cuda.Event()
-            with torch.cuda.stream(s_in):
-                if done_cmp[c] is not None:
-                    s_in.wait_event(done_cmp[c])
-                ps.g[lo:hi].copy_(g_host[lo:hi], non_blocking=True)
-                ev_in.record(s_in)
-            stream.wait_event(ev_in)
-            if done_out[c] is not None:
-                stream.wait_event(done_out[c])
-            asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
-            launches_e2e += 1
-            ev_c = torch.cuda.Event()
-            ev_c.record(stream)
-            done_cmp[c] = ev_c
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_c)
-                p_host[lo:hi].copy_(ps.p[lo:hi], non_blocking=True)
-                ev_o = torch.cuda.Event()
-                ev_o.record(s_out)
-            done_out[c] = ev_o
-    stream.wait_stream(s_in)
-    stream.wait_stream(s_out)
+    e2e_steps(e_steps)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -345,6 +398,8 @@ def run_gpu(args):
         rates, desc = cpu_oracle_sample(steps=3)
         cpu = {"value": statistics.median(rates) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": desc + ", median of 3 steps"}
+        cpu["all_cores"] = cpu_oracle_all_cores(pool, pool_cores)
+        pool.close()
 
     if rank == 0:
         line = {

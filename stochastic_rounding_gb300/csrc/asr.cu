@@ -40,7 +40,7 @@ namespace {
 // ------------------------------------------------------------------ config
 
 #ifndef ASR_THREADS
-#define ASR_THREADS 256
+#define ASR_THREADS 128
 #endif
 #ifndef ASR_UNROLL
 #define ASR_UNROLL 2
@@ -51,7 +51,7 @@ namespace {
 constexpr int kThreads = ASR_THREADS;       // threads per CTA
 constexpr int kVec = 8;                     // elements per unit (one 16 B bf16 vector)
 constexpr int kUnroll = ASR_UNROLL;         // units per thread per tile
-constexpr int kTile = kThreads * kVec * kUnroll;   // 4096 elements per tile
+constexpr int kTile = kThreads * kVec * kUnroll;   // 2048 elements per tile
 constexpr int kCapLarge = 512;              // descriptors per multi-tensor launch
 constexpr int kCapSmall = 1;                // single-tensor launch
 
