@@ -35,7 +35,10 @@ UNIT = "Gparams/s"
 BYTES_PER_PARAM = 22          # bf16 p r/w (2+2), bf16 g r (2), f32 m r/w (4+4), f32 v r/w (4+4)
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 NORTH_STAR_PEAK_GBS = 8000.0
-KERNEL_SRC = os.path.join(ROOT, "stochastic_rounding_gb300", "csrc", "asr.cu")
+# the device code of the AdamW-SR kernel: traffic figures are valid while
+# these files are unchanged
+KERNEL_SRC = [os.path.join(ROOT, "stochastic_rounding_gb300", "csrc", f)
+              for f in ("common.cuh", "pipeline.cuh", "adamw_kernels.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 CPU_SAMPLE_ELEMS = 1 << 24     # oracle sample per step (one core)
@@ -56,8 +59,11 @@ def measured_peak():
 
 
 def source_sha():
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for path in KERNEL_SRC:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def traffic_per_param():
@@ -236,6 +242,54 @@ def cpu_oracle_all_cores(pool, cores, per=1 << 23):
                       f"the oracle unchanged, sharded by base index"}
 
 
+def measure_configs(asr, W, dev, steps, warmup, peak):
+    """The other synthetic configurations, each timed with CUDA events after
+    warm-up: Gparams/s and algorithmic GB/s against the measured copy peak."""
+    import torch
+    out = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+
+    def timed(fn):
+        for t in range(1, warmup + 1):
+            fn(t)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for t in range(warmup + 1, warmup + steps + 1):
+            fn(t)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    def single(name, n, pdt, gdt, bpp, note):
+        p = W.device_normal_(torch.empty(n, dtype=pdt, device=dev), gen, 0.02)
+        g = W.device_normal_(torch.empty(n, dtype=gdt, device=dev), gen, 1e-3)
+        m = torch.zeros(n, device=dev)
+        v = torch.zeros(n, device=dev)
+        ms = timed(lambda t: asr.asr_adamw_sr_step(p, g, m, v, step=t, seed=0, **HP))
+        gbs = bpp * n / ms / 1e6
+        out[name] = {"params": n, "ms_per_step": ms, "gparams_per_s": n / ms / 1e6, "bytes_per_param": bpp,
+                     "gbs": gbs, "frac_of_measured_copy": gbs / peak, "note": note}
+        del p, g, m, v
+
+    single("single_65536_bf16", 65536, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM,
+           "1.4 MB: L2-resident and launch-bound")
+    single("fp32_16777216", 16777216, torch.float32, torch.float32, 28, "fp32 params and grads")
+    single("bf16_268435456", 268435456, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM, "one tensor")
+    ps = W.DeviceParamSet(W.LLAMA_1B, device=dev, seed=2)
+    from stochastic_rounding_gb300 import _lib
+    table = _lib.make_table(ps.tensors())
+    ms = timed(lambda t: asr.asr_adamw_sr_multi_tensor(table, step=t, seed=0, device=dev, **HP))
+    gbs = BYTES_PER_PARAM * ps.numel / ms / 1e6
+    out["llama_16L_h2048_147t"] = {"params": ps.numel, "ms_per_step": ms, "gparams_per_s": ps.numel / ms / 1e6,
+                                   "bytes_per_param": BYTES_PER_PARAM, "gbs": gbs,
+                                   "frac_of_measured_copy": gbs / peak, "note": "147 tensors, one launch"}
+    del ps
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -393,6 +447,11 @@ def run_gpu(args):
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
 
+    others = None
+    if rank == 0 and not args.params:
+        del g_host, p_host
+        others = measure_configs(asr, W, dev, args.steps, args.warmup, peak)
+
     cpu = None
     if rank == 0:
         rates, desc = cpu_oracle_sample(steps=3)
@@ -425,6 +484,7 @@ def run_gpu(args):
                     "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host; "
                             "chunks of consecutive tensors pipelined over three streams"},
             "gpu_launches": launches,
+            "configs": others,
             "clocks": clock,
         }
         print(json.dumps(line), flush=True)

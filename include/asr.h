@@ -14,8 +14,10 @@
  * Conventions shared by every entry point
  *   - Buffer pointers are DEVICE pointers (anything a kernel can dereference:
  *     cudaMalloc / torch CUDA memory, managed memory), owned by the caller.
- *     The library allocates no memory and keeps no state between calls apart
- *     from a per-device cache of the SM count and occupancy.
+ *     The library allocates no memory at run time.  What it keeps between
+ *     calls: per-device caches of launch shapes (and the tensor-map encoder's
+ *     address), a 4-byte device error word (asr_take_device_error) and the
+ *     static descriptor array of asr_adamw_sr_multi_tensor_static.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising the host.  Buffers
  *     must stay valid until the stream reaches the work.

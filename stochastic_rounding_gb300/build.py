@@ -13,7 +13,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "csrc", "asr.cu")
 HDR = os.path.join(ROOT, "include", "asr.h")
-INCLUDED = [os.path.join(HERE, "csrc", "gemm_sr.cuh")]     # textually included by asr.cu
+# textually included by asr.cu (one translation unit)
+INCLUDED = [os.path.join(HERE, "csrc", f) for f in (
+    "common.cuh", "pipeline.cuh", "adamw_kernels.cuh", "rounding_kernels.cuh", "static_table.cuh", "gemm_sr.cuh")]
 LIB = os.path.join(HERE, "libasr.so")
 
 NVCC_FLAGS = [

@@ -1,0 +1,336 @@
+// adamw_kernels.cuh -- the fused AdamW-SR kernels: the register-resident kernel
+// (any alignment) and the bulk-copy pipelined kernel (the hot path).
+// Included by asr.cu inside its anonymous namespace (one translation unit).
+
+// ------------------------------------------------------------ AdamW unit
+
+// Vector unit: eight elements at local offset e, all in range, all pointers
+// 16-byte aligned.  Loads are split from compute so a thread keeps several
+// units' loads in flight.
+template <int PT, int GT>
+struct VecUnit {
+    uint32_t p[PT == ASR_BF16 ? 4 : 8];
+    uint32_t g[GT == ASR_BF16 ? 4 : 8];
+    float m[8];
+    float v[8];
+};
+
+template <int PT, int GT>
+__device__ __forceinline__ void vec_load(const TensorEntry &T, uint64_t e, VecUnit<PT, GT> &u)
+{
+    if (PT == ASR_BF16) {
+        const uint4 a = ld_stream(static_cast<const uint16_t *>(T.p) + e);
+        u.p[0] = a.x; u.p[1] = a.y; u.p[2] = a.z; u.p[3] = a.w;
+    } else {
+        const float *pp = static_cast<const float *>(T.p) + e;
+        const uint4 a = ld_stream(pp), b = ld_stream(pp + 4);
+        u.p[0] = a.x; u.p[1] = a.y; u.p[2] = a.z; u.p[3] = a.w;
+        u.p[4] = b.x; u.p[5] = b.y; u.p[6] = b.z; u.p[7] = b.w;
+    }
+    if (GT == ASR_BF16) {
+        const uint4 a = ld_stream(static_cast<const uint16_t *>(T.g) + e);
+        u.g[0] = a.x; u.g[1] = a.y; u.g[2] = a.z; u.g[3] = a.w;
+    } else {
+        const float *gp = static_cast<const float *>(T.g) + e;
+        const uint4 a = ld_stream(gp), b = ld_stream(gp + 4);
+        u.g[0] = a.x; u.g[1] = a.y; u.g[2] = a.z; u.g[3] = a.w;
+        u.g[4] = b.x; u.g[5] = b.y; u.g[6] = b.z; u.g[7] = b.w;
+    }
+    {
+        const uint4 a = ld_stream(T.m + e), b = ld_stream(T.m + e + 4);
+        u.m[0] = __uint_as_float(a.x); u.m[1] = __uint_as_float(a.y);
+        u.m[2] = __uint_as_float(a.z); u.m[3] = __uint_as_float(a.w);
+        u.m[4] = __uint_as_float(b.x); u.m[5] = __uint_as_float(b.y);
+        u.m[6] = __uint_as_float(b.z); u.m[7] = __uint_as_float(b.w);
+    }
+    {
+        const uint4 a = ld_stream(T.v + e), b = ld_stream(T.v + e + 4);
+        u.v[0] = __uint_as_float(a.x); u.v[1] = __uint_as_float(a.y);
+        u.v[2] = __uint_as_float(a.z); u.v[3] = __uint_as_float(a.w);
+        u.v[4] = __uint_as_float(b.x); u.v[5] = __uint_as_float(b.y);
+        u.v[6] = __uint_as_float(b.z); u.v[7] = __uint_as_float(b.w);
+    }
+}
+
+template <int PT, int GT>
+__device__ __forceinline__ float vec_p(const VecUnit<PT, GT> &u, int k)
+{
+    if (PT == ASR_BF16) return (k & 1) ? bf16_hi(u.p[k >> 1]) : bf16_lo(u.p[k >> 1]);
+    return __uint_as_float(u.p[k]);
+}
+
+template <int PT, int GT>
+__device__ __forceinline__ float vec_g(const VecUnit<PT, GT> &u, int k)
+{
+    if (GT == ASR_BF16) return (k & 1) ? bf16_hi(u.g[k >> 1]) : bf16_lo(u.g[k >> 1]);
+    return __uint_as_float(u.g[k]);
+}
+
+template <int PT, int GT, int RM>
+__device__ __forceinline__ void vec_compute_store(const TensorEntry &T, uint64_t e, VecUnit<PT, GT> &u,
+                                                  const AdamParams &P)
+{
+    float pn[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pn[k] = adamw_elem(vec_p(u, k), vec_g(u, k), u.m[k], u.v[k], P.s);
+
+    if (PT == ASR_BF16) {
+        uint32_t w[4];
+        if (RM == ASR_ROUND_SR) {
+            uint32_t r[8];
+            unit_words<true>(T.base, e, P.step, P.keys, r);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = sr_pack2<ASR_ADAMW_CVT_RS>(pn[2 * k], pn[2 * k + 1], r[2 * k], r[2 * k + 1]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = pack_bf16(round_rne(pn[2 * k]), round_rne(pn[2 * k + 1]));
+        }
+        st_stream(static_cast<uint16_t *>(T.p) + e, make_uint4(w[0], w[1], w[2], w[3]));
+    } else {
+        float *pp = static_cast<float *>(T.p) + e;
+        st_stream(pp, make_uint4(__float_as_uint(pn[0]), __float_as_uint(pn[1]), __float_as_uint(pn[2]),
+                                 __float_as_uint(pn[3])));
+        st_stream(pp + 4, make_uint4(__float_as_uint(pn[4]), __float_as_uint(pn[5]), __float_as_uint(pn[6]),
+                                     __float_as_uint(pn[7])));
+    }
+    st_stream(T.m + e, make_uint4(__float_as_uint(u.m[0]), __float_as_uint(u.m[1]), __float_as_uint(u.m[2]),
+                                  __float_as_uint(u.m[3])));
+    st_stream(T.m + e + 4, make_uint4(__float_as_uint(u.m[4]), __float_as_uint(u.m[5]),
+                                      __float_as_uint(u.m[6]), __float_as_uint(u.m[7])));
+    st_stream(T.v + e, make_uint4(__float_as_uint(u.v[0]), __float_as_uint(u.v[1]), __float_as_uint(u.v[2]),
+                                  __float_as_uint(u.v[3])));
+    st_stream(T.v + e + 4, make_uint4(__float_as_uint(u.v[4]), __float_as_uint(u.v[5]),
+                                      __float_as_uint(u.v[6]), __float_as_uint(u.v[7])));
+}
+
+// Scalar unit: local elements e..min(e+8, n)-1, any alignment, any base.
+template <int PT, int GT, int RM>
+__device__ __forceinline__ void scalar_unit(const TensorEntry &T, uint64_t e, const AdamParams &P)
+{
+    uint32_t r[8];
+    if (PT == ASR_BF16 && RM == ASR_ROUND_SR) unit_words<false>(T.base, e, P.step, P.keys, r);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint64_t j = e + k;
+        if (j >= T.n) break;
+        const float p = PT == ASR_BF16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(T.p)[j]) << 16)
+                                       : static_cast<const float *>(T.p)[j];
+        const float g = GT == ASR_BF16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(T.g)[j]) << 16)
+                                       : static_cast<const float *>(T.g)[j];
+        float m = T.m[j], v = T.v[j];
+        const float pn = adamw_elem(p, g, m, v, P.s);
+        T.m[j] = m;
+        T.v[j] = v;
+        if (PT == ASR_BF16) {
+            const uint32_t h = RM == ASR_ROUND_SR ? round_sr(pn, r[k]) : round_rne(pn);
+            static_cast<uint16_t *>(T.p)[j] = static_cast<uint16_t>(h);
+        } else {
+            static_cast<float *>(T.p)[j] = pn;
+        }
+    }
+}
+
+// Persistent grid-stride kernel over the tiles of every tensor in the table.
+// FAST: every tensor has 16-byte-aligned buffers and base % 4 == 0.
+template <int PT, int GT, int RM, bool FAST, int CAP>
+__global__ void __launch_bounds__(kThreads, ASR_MIN_BLOCKS)
+adamw_sr_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P)
+{
+    int t = 0;
+    for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x) {
+        while (tile >= tab.t[t].tile_end) ++t;
+        const TensorEntry &T = tab.t[t];
+        const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
+        const uint64_t off = (tile - first) * static_cast<uint64_t>(kTile);
+        if (FAST && off + kTile <= T.n) {
+            VecUnit<PT, GT> u[kUnroll];
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k)
+                vec_load(T, off + (static_cast<uint64_t>(k) * kThreads + threadIdx.x) * kVec, u[k]);
+#pragma unroll
+            for (int k = 0; k < kUnroll; ++k)
+                vec_compute_store<PT, GT, RM>(T, off + (static_cast<uint64_t>(k) * kThreads + threadIdx.x) * kVec,
+                                              u[k], P);
+        } else {
+#pragma unroll 1
+            for (int k = 0; k < kUnroll; ++k) {
+                const uint64_t e = off + (static_cast<uint64_t>(k) * kThreads + threadIdx.x) * kVec;
+                if (e >= T.n) break;
+                if (FAST && e + kVec <= T.n) {
+                    VecUnit<PT, GT> one;
+                    vec_load(T, e, one);
+                    vec_compute_store<PT, GT, RM>(T, e, one, P);
+                } else {
+                    scalar_unit<PT, GT, RM>(T, e, P);
+                }
+            }
+        }
+    }
+}
+
+template <int PT, int GT>
+struct TmaStage {
+    static constexpr int kPBytes = kTmaTile * (PT == ASR_BF16 ? 2 : 4);
+    static constexpr int kGBytes = kTmaTile * (GT == ASR_BF16 ? 2 : 4);
+    static constexpr int kMBytes = kTmaTile * 4;
+    static constexpr int kBytes = kPBytes + kGBytes + 2 * kMBytes;
+    // as many stages as fit in the shared-memory budget, at most ASR_TMA_STAGES
+    static constexpr int kFit = ASR_TMA_SMEM_KB * 1024 / kBytes;
+    static constexpr int kStages = kFit < ASR_TMA_STAGES ? kFit : ASR_TMA_STAGES;
+    static_assert(kStages >= 2, "need at least two stages");
+    static constexpr int kSmem = kStages * kBytes + 2 * kStages * 8 + kTmaConsumerWarps * 4;
+};
+
+// Locate tile `tile` of the table, advancing the cursor t.
+template <int CAP>
+__device__ __forceinline__ void find_tile(const AdamTable<CAP> &tab, uint64_t tile, int &t, uint64_t &off,
+                                          uint32_t &cnt)
+{
+    while (tile >= tab.t[t].tile_end) ++t;
+    const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
+    off = (tile - first) * static_cast<uint64_t>(kTmaTile);
+    const uint64_t rest = tab.t[t].n - off;
+    cnt = rest < static_cast<uint64_t>(kTmaTile) ? static_cast<uint32_t>(rest) : static_cast<uint32_t>(kTmaTile);
+}
+
+// All tensors FAST (16-byte-aligned buffers, base % 4 == 0); tile size kTmaTile.
+template <int PT, int GT, int RM, int CAP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P,
+                    uint64_t limit_ns)
+{
+    using S = TmaStage<PT, GT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bars = sbase + S::kStages * S::kBytes;      // full[s] then empty[s]
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (S::kStages + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kTmaConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == kTmaConsumerWarps) {
+        // ------------------------------------------------------ producer
+        if (lane != 0) return;
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        int t = 0;
+        uint32_t k = 0;
+        for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+            const int s = static_cast<int>(k % S::kStages);
+            const uint32_t use = k / S::kStages;
+            if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
+            uint64_t off;
+            uint32_t cnt;
+            find_tile(tab, tile, t, off, cnt);
+            const TensorEntry &T = tab.t[t];
+            const uint32_t c8 = cnt & ~7u;
+            const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
+            const uint32_t mb = c8 * 4u;
+            mbar_arrive_expect_tx(full(s), pb + gb + 2 * mb);
+            if (c8) {
+                const uint32_t dst = sbase + s * S::kBytes;
+                bulk_load(dst, static_cast<const unsigned char *>(T.p) + off * (PT == ASR_BF16 ? 2 : 4), pb,
+                          full(s), policy);
+                bulk_load(dst + S::kPBytes, static_cast<const unsigned char *>(T.g) + off * (GT == ASR_BF16 ? 2 : 4),
+                          gb, full(s), policy);
+                bulk_load(dst + S::kPBytes + S::kGBytes, T.m + off, mb, full(s), policy);
+                bulk_load(dst + S::kPBytes + S::kGBytes + S::kMBytes, T.v + off, mb, full(s), policy);
+            }
+        }
+        // Every copy this thread issued must land before the CTA may exit:
+        // wait (bounded) for the last use of each stage.
+        const uint32_t issued = k;
+        for (int s = 0; s < S::kStages; ++s) {
+            if (static_cast<uint32_t>(s) >= issued) break;
+            const uint32_t last_use = (issued - 1 - s) / S::kStages;
+            mbar_wait(full(s), last_use & 1u, limit_ns);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ct = threadIdx.x;            // 0 .. kTmaConsumers-1
+    const uint32_t dep_slot = bars + 16u * S::kStages + 4u * warp;   // one word per consumer warp
+    int t = 0;
+    uint32_t k = 0;
+    for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % S::kStages);
+        const uint32_t use = k / S::kStages;
+        if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
+        uint64_t off;
+        uint32_t cnt;
+        find_tile(tab, tile, t, off, cnt);
+        const TensorEntry &T = tab.t[t];
+        const uint32_t c8 = cnt & ~7u;
+        const unsigned char *st = smem + s * S::kBytes;
+        VecUnit<PT, GT> u[kTmaUnits];
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8) {
+                if (PT == ASR_BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 2);
+                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 4);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(st + e * 4 + 16);
+                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
+                    u[j].p[4] = b.x; u[j].p[5] = b.y; u[j].p[6] = b.z; u[j].p[7] = b.w;
+                }
+                const unsigned char *gs = st + S::kPBytes;
+                if (GT == ASR_BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 2);
+                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 4);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(gs + e * 4 + 16);
+                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
+                    u[j].g[4] = b.x; u[j].g[5] = b.y; u[j].g[6] = b.z; u[j].g[7] = b.w;
+                }
+                const float4 *ms = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + e * 4);
+                const float4 *vs = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + S::kMBytes + e * 4);
+                const float4 m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1];
+                u[j].m[0] = m0.x; u[j].m[1] = m0.y; u[j].m[2] = m0.z; u[j].m[3] = m0.w;
+                u[j].m[4] = m1.x; u[j].m[5] = m1.y; u[j].m[6] = m1.z; u[j].m[7] = m1.w;
+                u[j].v[0] = v0.x; u[j].v[1] = v0.y; u[j].v[2] = v0.z; u[j].v[3] = v0.w;
+                u[j].v[4] = v1.x; u[j].v[5] = v1.y; u[j].v[6] = v1.z; u[j].v[7] = v1.w;
+            }
+        }
+        // Hand the stage back only once this warp's shared-memory loads have
+        // returned (the next bulk copy into the stage would otherwise race
+        // with a load still queued): every lane folds one register of each
+        // 128-bit load into `dep` and stores it; in-order issue holds that
+        // store, and so the warp barrier and the release after it, until
+        // every folded load is back.
+        uint32_t dep = 0;
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8)
+                dep ^= u[j].p[0] ^ u[j].g[0] ^ __float_as_uint(u[j].m[0]) ^ __float_as_uint(u[j].m[4]) ^
+                       __float_as_uint(u[j].v[0]) ^ __float_as_uint(u[j].v[4]) ^
+                       (PT == ASR_BF16 ? 0u : u[j].p[4]) ^ (GT == ASR_BF16 ? 0u : u[j].g[4]);
+        }
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dep_slot), "r"(dep) : "memory");
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(empty(s));
+        }
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
+        }
+        // a ragged end of a tensor (< 8 elements) goes through the scalar path
+        if (c8 < cnt && ct == (c8 / kVec) % kTmaConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
+    }
+}

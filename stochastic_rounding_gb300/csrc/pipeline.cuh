@@ -1,0 +1,139 @@
+// pipeline.cuh -- the shared-memory pipeline machinery: bulk-copy (TMA)
+// configuration, the library's device error word, the bounded mbarrier waits
+// and their self-test kernel.
+// Included by asr.cu inside its anonymous namespace (one translation unit).
+
+// --------------------------------------------- bulk-copy pipelined kernel
+//
+// The same step, with the loads taken off the registers: a producer warp
+// streams every tile's p, g, m and v into a ring of shared-memory stages with
+// cp.async.bulk (the Blackwell/Hopper bulk-copy engine; completion counted on
+// an mbarrier), while consumer warps compute from shared memory and store
+// their results straight to global memory.  With several 48 KB stages in
+// flight per SM the kernel keeps far more bytes outstanding than register
+// occupancy allows.
+//
+// Every mbarrier wait is bounded by a %globaltimer limit; a wait that gives
+// up sets a bit in g_device_error, the thread leaves its loop, and the
+// producer still waits (bounded) for the copies it issued before exiting.
+
+#ifndef ASR_TMA_STAGES
+#define ASR_TMA_STAGES 4
+#endif
+#ifndef ASR_TMA_CONSUMER_WARPS
+#define ASR_TMA_CONSUMER_WARPS 20
+#endif
+#ifndef ASR_TMA_SMEM_KB
+#define ASR_TMA_SMEM_KB 200
+#endif
+#ifndef ASR_TMA_EVICT_FIRST
+#define ASR_TMA_EVICT_FIRST 1
+#endif
+#ifndef ASR_TMA_TILE
+#define ASR_TMA_TILE 5120
+#endif
+constexpr int kTmaTile = ASR_TMA_TILE;
+constexpr int kTmaConsumerWarps = ASR_TMA_CONSUMER_WARPS;
+constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
+constexpr int kTmaThreads = kTmaConsumers + 32;        // + one producer warp
+constexpr int kTmaUnits = kTmaTile / kVec / kTmaConsumers;   // units per consumer thread per tile
+static_assert(kTmaUnits >= 1 && kTmaUnits * kTmaConsumers * kVec == kTmaTile, "tile must split evenly");
+constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: a healthy wait takes microseconds
+
+constexpr uint32_t kErrWaitTimeout = 1u;
+
+__device__ unsigned int g_device_error = 0;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the phase with the given parity has completed, for at most
+// limit_ns.  Returns false (and raises the device error bit) on timeout.
+// A second guard caps the number of polls, so the wait ends even if the
+// timer did not advance.
+constexpr uint32_t kWaitMaxPolls = 1u << 26;
+
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t polls = 0; !mbar_test(bar, parity); ++polls) {
+        if (global_ns() - t0 > limit_ns || polls >= kWaitMaxPolls) {
+            atomicOr(&g_device_error, kErrWaitTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_test(bar, parity)) return true;      // fast path: already complete
+    return mbar_wait_bounded(bar, parity, limit_ns);
+}
+
+// Diagnostic: one thread waits, with the given limit, on a barrier that
+// nothing arrives on, so the bounded wait must give up and raise the error
+// bit.  Shows that a stuck pipeline ends with a readable status.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(b, 0, limit_ns);
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy)
+{
+#if ASR_TMA_EVICT_FIRST
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+#else
+    (void)policy;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+#endif
+}

@@ -1,0 +1,358 @@
+// static_table.cuh -- the allocation-free multi-tensor step (its descriptor
+// table in a library-owned static device array) and its host launcher.
+// Included by asr.cu inside its anonymous namespace (one translation unit).
+
+// ------------------------------------------ allocation-free multi-tensor step
+//
+// A variant of the bulk-copy pipelined step for callers that must not
+// allocate device memory.  Its scratch -- the tensor descriptor table the
+// kernel walks -- lives in a file-scope device array owned by the library,
+// so one launch per dtype group covers up to kStaticTableMax tensors without
+// anyone calling cudaMalloc.  Every device that loads the library holds the
+// array until the process exits.  Each call rewrites the part of the array it
+// uses, so nothing in it has to start at zero; calls whose kernels overlap on
+// the GPU (other streams, other host threads) share the array and race.
+
+constexpr int kStaticTableMax = ASR_STATIC_TABLE_MAX;   // 4096 descriptors x 56 B = 224 KB per device
+
+static __device__ __align__(256) TensorEntry g_static_table[kStaticTableMax];
+
+struct GlobalTable {
+    const TensorEntry *t;       // device address inside g_static_table
+    uint64_t total_tiles;
+};
+
+__device__ __forceinline__ void find_tile(const GlobalTable &tab, uint64_t tile, int &t, uint64_t &off,
+                                          uint32_t &cnt)
+{
+    while (tile >= tab.t[t].tile_end) ++t;
+    const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
+    off = (tile - first) * static_cast<uint64_t>(kTmaTile);
+    const uint64_t rest = tab.t[t].n - off;
+    cnt = rest < static_cast<uint64_t>(kTmaTile) ? static_cast<uint32_t>(rest) : static_cast<uint32_t>(kTmaTile);
+}
+
+// The pipeline of adamw_sr_tma_kernel, with the table read from global memory.
+template <int PT, int GT, int RM>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid_constant__ AdamParams P,
+                           uint64_t limit_ns)
+{
+    using S = TmaStage<PT, GT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bars = sbase + S::kStages * S::kBytes;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (S::kStages + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S::kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kTmaConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == kTmaConsumerWarps) {
+        if (lane != 0) return;
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        int t = 0;
+        uint32_t k = 0;
+        for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+            const int s = static_cast<int>(k % S::kStages);
+            const uint32_t use = k / S::kStages;
+            if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
+            uint64_t off;
+            uint32_t cnt;
+            find_tile(tab, tile, t, off, cnt);
+            const TensorEntry &T = tab.t[t];
+            const uint32_t c8 = cnt & ~7u;
+            const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
+            const uint32_t mb = c8 * 4u;
+            mbar_arrive_expect_tx(full(s), pb + gb + 2 * mb);
+            if (c8) {
+                const uint32_t dst = sbase + s * S::kBytes;
+                bulk_load(dst, static_cast<const unsigned char *>(T.p) + off * (PT == ASR_BF16 ? 2 : 4), pb,
+                          full(s), policy);
+                bulk_load(dst + S::kPBytes, static_cast<const unsigned char *>(T.g) + off * (GT == ASR_BF16 ? 2 : 4),
+                          gb, full(s), policy);
+                bulk_load(dst + S::kPBytes + S::kGBytes, T.m + off, mb, full(s), policy);
+                bulk_load(dst + S::kPBytes + S::kGBytes + S::kMBytes, T.v + off, mb, full(s), policy);
+            }
+        }
+        // every copy issued here must land before the CTA exits
+        const uint32_t issued = k;
+        for (int s = 0; s < S::kStages; ++s) {
+            if (static_cast<uint32_t>(s) >= issued) break;
+            const uint32_t last_use = (issued - 1 - s) / S::kStages;
+            mbar_wait(full(s), last_use & 1u, limit_ns);
+        }
+        return;
+    }
+
+    const int ct = threadIdx.x;
+    const uint32_t dep_slot = bars + 16u * S::kStages + 4u * warp;
+    int t = 0;
+    uint32_t k = 0;
+    for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+        const int s = static_cast<int>(k % S::kStages);
+        const uint32_t use = k / S::kStages;
+        if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
+        uint64_t off;
+        uint32_t cnt;
+        find_tile(tab, tile, t, off, cnt);
+        const TensorEntry &T = tab.t[t];
+        const uint32_t c8 = cnt & ~7u;
+        const unsigned char *st = smem + s * S::kBytes;
+        VecUnit<PT, GT> u[kTmaUnits];
+        uint32_t dep = 0;
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8) {
+                if (PT == ASR_BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 2);
+                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 4);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(st + e * 4 + 16);
+                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
+                    u[j].p[4] = b.x; u[j].p[5] = b.y; u[j].p[6] = b.z; u[j].p[7] = b.w;
+                }
+                const unsigned char *gs = st + S::kPBytes;
+                if (GT == ASR_BF16) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 2);
+                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
+                } else {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 4);
+                    const uint4 b = *reinterpret_cast<const uint4 *>(gs + e * 4 + 16);
+                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
+                    u[j].g[4] = b.x; u[j].g[5] = b.y; u[j].g[6] = b.z; u[j].g[7] = b.w;
+                }
+                const float4 *ms = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + e * 4);
+                const float4 *vs = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + S::kMBytes + e * 4);
+                const float4 m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1];
+                u[j].m[0] = m0.x; u[j].m[1] = m0.y; u[j].m[2] = m0.z; u[j].m[3] = m0.w;
+                u[j].m[4] = m1.x; u[j].m[5] = m1.y; u[j].m[6] = m1.z; u[j].m[7] = m1.w;
+                u[j].v[0] = v0.x; u[j].v[1] = v0.y; u[j].v[2] = v0.z; u[j].v[3] = v0.w;
+                u[j].v[4] = v1.x; u[j].v[5] = v1.y; u[j].v[6] = v1.z; u[j].v[7] = v1.w;
+                dep ^= u[j].p[0] ^ u[j].g[0] ^ __float_as_uint(m0.x) ^ __float_as_uint(m1.x) ^
+                       __float_as_uint(v0.x) ^ __float_as_uint(v1.x) ^ (PT == ASR_BF16 ? 0u : u[j].p[4]) ^
+                       (GT == ASR_BF16 ? 0u : u[j].g[4]);
+            }
+        }
+        // release the stage only after this warp's loads have returned
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dep_slot), "r"(dep) : "memory");
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(empty(s));
+        }
+#pragma unroll
+        for (int j = 0; j < kTmaUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+            if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
+        }
+        if (c8 < cnt && ct == (c8 / kVec) % kTmaConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
+    }
+}
+
+// Per-device set-up of this path, kept in fixed arrays (no allocation): the
+// device address of g_static_table -- on the host its name is only a
+// stand-in for the symbol, so the address is looked up with
+// cudaGetSymbolAddress while the device is current -- and the persistent grid
+// of each kernel variant.
+constexpr int kMaxDevices = 64;
+constexpr int kStaticVariants = 12;        // 6 dtype/rounding combinations x {pipelined, plain}
+std::mutex g_static_mu;
+TensorEntry *g_static_addr[kMaxDevices];
+int g_static_grid[kMaxDevices][kStaticVariants];
+
+asr_status static_device(int *dev_out, TensorEntry **table_out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ASR_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_static_table);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_static_addr[dev] = static_cast<TensorEntry *>(ptr);
+    }
+    *dev_out = dev;
+    *table_out = g_static_addr[dev];
+    return ASR_OK;
+}
+
+template <typename K>
+asr_status static_grid(K kernel, int dev, int slot, int threads, int smem, int *grid)
+{
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (g_static_grid[dev][slot] == 0) {
+        cudaError_t e = cudaSuccess;
+        if (smem > 48 * 1024) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        int sms = 0, per_sm = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_static_grid[dev][slot] = sms * (per_sm < 1 ? 1 : per_sm);
+    }
+    *grid = g_static_grid[dev][slot];
+    return ASR_OK;
+}
+
+constexpr int variant_slot(int pdt, int gdt, int rm) { return pdt == ASR_BF16 ? gdt * 2 + rm : 4 + gdt; }
+
+// Host staging: fixed arrays, guarded by a mutex for the duration of a call.
+std::mutex g_stage_mu;
+TensorEntry g_stage_table[kStaticTableMax];
+AdamTable<kCapLarge> g_stage_plain;
+
+template <int PT, int GT, int RM>
+asr_status launch_static_group(int dev, const TensorEntry *dev_table, uint64_t tiles, const AdamParams &P,
+                               cudaStream_t stream)
+{
+    auto kernel = adamw_sr_tma_static_kernel<PT, GT, RM>;
+    const int smem = TmaStage<PT, GT>::kSmem;
+    int grid = 0;
+    asr_status st = static_grid(kernel, dev, variant_slot(PT, GT, RM), kTmaThreads, smem, &grid);
+    if (st != ASR_OK) return st;
+    if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
+    GlobalTable tab;
+    tab.t = dev_table;
+    tab.total_tiles = tiles;
+    kernel<<<grid, kTmaThreads, smem, stream>>>(tab, P, kWaitLimitNs);
+    return check_launch();
+}
+
+// Tensors that are not vector-eligible take the plain kernel, its table in
+// the launch parameters (staged in g_stage_plain, kCapLarge per launch).
+template <int PT, int GT, int RM>
+asr_status launch_static_plain(int dev, const asr_tensor_desc *table, int32_t n_tensors, const AdamParams &P,
+                               cudaStream_t stream)
+{
+    int32_t i = 0;
+    int grid = 0;
+    while (i < n_tensors) {
+        int c = 0;
+        uint64_t tiles = 0;
+        for (; i < n_tensors && c < kCapLarge; ++i) {
+            const asr_tensor_desc &d = table[i];
+            if (d.n == 0 || d.param_dtype != PT || d.grad_dtype != GT || desc_fast(d)) continue;
+            TensorEntry &T = g_stage_plain.t[c++];
+            T.p = d.param;
+            T.g = d.grad;
+            T.m = d.exp_avg;
+            T.v = d.exp_avg_sq;
+            T.n = d.n;
+            T.base = d.base_index;
+            tiles += (d.n + kTile - 1) / kTile;
+            T.tile_end = tiles;
+        }
+        if (c == 0) continue;
+        auto kernel = adamw_sr_kernel<PT, GT, RM, false, kCapLarge>;
+        if (grid == 0) {
+            asr_status st = static_grid(kernel, dev, 6 + variant_slot(PT, GT, RM), kThreads, 0, &grid);
+            if (st != ASR_OK) return st;
+        }
+        g_stage_plain.total_tiles = tiles;
+        g_stage_plain.count = c;
+        const int g = static_cast<uint64_t>(grid) > tiles ? static_cast<int>(tiles) : grid;
+        kernel<<<g, kThreads, 0, stream>>>(g_stage_plain, P);
+        asr_status st = check_launch();
+        if (st != ASR_OK) return st;
+    }
+    return ASR_OK;
+}
+
+template <int PT, int GT, int RM>
+asr_status launch_static_combo(int dev, const TensorEntry *dev_table, uint64_t tiles, bool any_vector,
+                               const asr_tensor_desc *table, int32_t n_tensors, const AdamParams &P,
+                               cudaStream_t stream)
+{
+    if (any_vector) {
+        asr_status st = launch_static_group<PT, GT, RM>(dev, dev_table, tiles, P, stream);
+        if (st != ASR_OK) return st;
+    }
+    return launch_static_plain<PT, GT, RM>(dev, table, n_tensors, P, stream);
+}
+
+asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, const asr_adamw_hparams *hp,
+                            cudaStream_t stream)
+{
+    asr_status st = validate_hparams(hp);
+    if (st != ASR_OK) return st;
+    if (n_tensors < 0 || n_tensors > kStaticTableMax || (n_tensors > 0 && !table)) return ASR_ERR_INVALID_VALUE;
+    for (int32_t i = 0; i < n_tensors; ++i) {
+        st = validate_desc(table[i]);
+        if (st != ASR_OK) return st;
+    }
+    if (n_tensors == 0) return ASR_OK;
+    int dev = 0;
+    TensorEntry *dev_table = nullptr;
+    st = static_device(&dev, &dev_table);
+    if (st != ASR_OK) return st;
+    AdamParams P;
+    P.s = make_scalars(*hp);
+    P.keys = make_keys(hp->seed);
+    P.step = hp->step;
+    const int rm = static_cast<int>(hp->rounding);
+
+    std::lock_guard<std::mutex> lk(g_stage_mu);
+    // Vector-eligible tensors: one contiguous block of the table per dtype
+    // group (group index = param dtype * 2 + grad dtype), sent in one copy.
+    int used = 0;
+    int group_start[4] = {0, 0, 0, 0}, group_count[4] = {0, 0, 0, 0};
+    uint64_t group_tiles[4] = {0, 0, 0, 0};
+    for (int gi = 0; gi < 4; ++gi) {
+        const int pdt = gi / 2, gdt = gi % 2;
+        group_start[gi] = used;
+        uint64_t tiles = 0;
+        for (int32_t i = 0; i < n_tensors; ++i) {
+            const asr_tensor_desc &d = table[i];
+            if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || !desc_fast(d)) continue;
+            TensorEntry &T = g_stage_table[used++];
+            T.p = d.param;
+            T.g = d.grad;
+            T.m = d.exp_avg;
+            T.v = d.exp_avg_sq;
+            T.n = d.n;
+            T.base = d.base_index;
+            tiles += (d.n + kTmaTile - 1) / kTmaTile;
+            T.tile_end = tiles;
+        }
+        group_count[gi] = used - group_start[gi];
+        group_tiles[gi] = tiles;
+    }
+    if (used > 0) {
+        // From pageable host memory: returns once the table is staged for the
+        // transfer, which the kernels below follow on the same stream.
+        cudaError_t e = cudaMemcpyAsync(dev_table, g_stage_table, sizeof(TensorEntry) * used,
+                                        cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    for (int gi = 0; gi < 4; ++gi) {
+        const bool any = group_count[gi] > 0;
+        const TensorEntry *tb = dev_table + group_start[gi];
+        const uint64_t tl = group_tiles[gi];
+        if (gi == 3)        // bf16 params, bf16 grads
+            st = rm == ASR_ROUND_SR
+                ? launch_static_combo<ASR_BF16, ASR_BF16, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream)
+                : launch_static_combo<ASR_BF16, ASR_BF16, ASR_ROUND_RNE>(dev, tb, tl, any, table, n_tensors, P, stream);
+        else if (gi == 2)   // bf16 params, f32 grads
+            st = rm == ASR_ROUND_SR
+                ? launch_static_combo<ASR_BF16, ASR_F32, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream)
+                : launch_static_combo<ASR_BF16, ASR_F32, ASR_ROUND_RNE>(dev, tb, tl, any, table, n_tensors, P, stream);
+        else if (gi == 1)   // f32 params, bf16 grads (the rounding mode does not apply)
+            st = launch_static_combo<ASR_F32, ASR_BF16, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream);
+        else                // f32 params, f32 grads
+            st = launch_static_combo<ASR_F32, ASR_F32, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream);
+        if (st != ASR_OK) return st;
+    }
+    return ASR_OK;
+}
