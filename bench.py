@@ -176,6 +176,24 @@ def cpu_oracle_sample(steps, sample_elems=CPU_SAMPLE_ELEMS, seed=0):
     return rates, desc
 
 
+def pinned_bf16(n):
+    """An n-element bf16 host tensor in page-locked memory of exactly that
+    size (torch's pinned allocator rounds each request up to a power of two,
+    which for the 16 GB buffers here would double the host memory taken)."""
+    import numpy as np
+    import torch
+    arr = np.empty(2 * n, dtype=np.uint8)
+    rc = torch.cuda.cudart().cudaHostRegister(arr.ctypes.data, arr.nbytes, 0)
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister failed ({rc})")
+    return torch.from_numpy(arr).view(torch.bfloat16), arr
+
+
+def unpin(arr):
+    import torch
+    torch.cuda.cudart().cudaHostUnregister(arr.ctypes.data)
+
+
 def e2e_chunks(tensors, offset, max_params=1 << 28):
     """Consecutive tensors grouped into chunks of at most max_params (a larger
     tensor is a chunk of its own).  Each chunk is a contiguous range [lo, hi)
@@ -392,8 +410,8 @@ def run_gpu(args):
     # out.  Chunks of consecutive tensors (contiguous ranges of the flat
     # buffers) are pipelined over three streams: H2D of chunk c+1 and D2H of
     # chunk c-1 overlap the multi-tensor call on chunk c.
-    g_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
-    p_host = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+    g_host, g_arr = pinned_bf16(n)
+    p_host, p_arr = pinned_bf16(n)
     g_host.copy_(ps.g)
     chunks = e2e_chunks(tensors, offset)
     s_in = torch.cuda.Stream(device=dev)
@@ -446,10 +464,12 @@ def run_gpu(args):
     barrier()
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
+    del g_host, p_host
+    unpin(g_arr)
+    unpin(p_arr)
 
     others = None
     if rank == 0 and not args.params:
-        del g_host, p_host
         others = measure_configs(asr, W, dev, args.steps, args.warmup, peak)
 
     cpu = None
