@@ -176,24 +176,6 @@ def cpu_oracle_sample(steps, sample_elems=CPU_SAMPLE_ELEMS, seed=0):
     return rates, desc
 
 
-def pinned_bf16(n):
-    """An n-element bf16 host tensor in page-locked memory of exactly that
-    size (torch's pinned allocator rounds each request up to a power of two,
-    which for the 16 GB buffers here would double the host memory taken)."""
-    import numpy as np
-    import torch
-    arr = np.empty(2 * n, dtype=np.uint8)
-    rc = torch.cuda.cudart().cudaHostRegister(arr.ctypes.data, arr.nbytes, 0)
-    if int(rc) != 0:
-        raise RuntimeError(f"cudaHostRegister failed ({rc})")
-    return torch.from_numpy(arr).view(torch.bfloat16), arr
-
-
-def unpin(arr):
-    import torch
-    torch.cuda.cudart().cudaHostUnregister(arr.ctypes.data)
-
-
 def e2e_chunks(tensors, offset, max_params=1 << 28):
     """Consecutive tensors grouped into chunks of at most max_params (a larger
     tensor is a chunk of its own).  Each chunk is a contiguous range [lo, hi)
@@ -410,10 +392,14 @@ def run_gpu(args):
     # out.  Chunks of consecutive tensors (contiguous ranges of the flat
     # buffers) are pipelined over three streams: H2D of chunk c+1 and D2H of
     # chunk c-1 overlap the multi-tensor call on chunk c.
-    g_host, g_arr = pinned_bf16(n)
-    p_host, p_arr = pinned_bf16(n)
-    g_host.copy_(ps.g)
     chunks = e2e_chunks(tensors, offset)
+    # one pinned host buffer per chunk: torch's pinned allocator rounds each
+    # request up to a power of two, which for two whole 16 GB buffers would
+    # double the host memory taken; per ~512 MB chunk the rounding wastes ~10 %
+    g_host = [torch.empty(hi - lo, dtype=torch.bfloat16, pin_memory=True) for lo, hi, _ in chunks]
+    p_host = [torch.empty(hi - lo, dtype=torch.bfloat16, pin_memory=True) for lo, hi, _ in chunks]
+    for (lo, hi, _), gh in zip(chunks, g_host):
+        gh.copy_(ps.g[lo:hi])
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
     done_cmp = [None] * len(chunks)          # compute of chunk c finished (grads free)
@@ -431,7 +417,7 @@ def run_gpu(args):
                 with torch.cuda.stream(s_in):
                     if done_cmp[c] is not None:
                         s_in.wait_event(done_cmp[c])
-                    ps.g[lo:hi].copy_(g_host[lo:hi], non_blocking=True)
+                    ps.g[lo:hi].copy_(g_host[c], non_blocking=True)
                     ev_in.record(s_in)
                 stream.wait_event(ev_in)
                 if done_out[c] is not None:
@@ -443,7 +429,7 @@ def run_gpu(args):
                 done_cmp[c] = ev_c
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_c)
-                    p_host[lo:hi].copy_(ps.p[lo:hi], non_blocking=True)
+                    p_host[c].copy_(ps.p[lo:hi], non_blocking=True)
                     ev_o = torch.cuda.Event()
                     ev_o.record(s_out)
                 done_out[c] = ev_o
@@ -465,8 +451,6 @@ def run_gpu(args):
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
     del g_host, p_host
-    unpin(g_arr)
-    unpin(p_arr)
 
     others = None
     if rank == 0 and not args.params:

@@ -170,36 +170,40 @@ adamw_sr_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constan
 
 template <int PT, int GT>
 struct TmaStage {
-    static constexpr int kPBytes = kTmaTile * (PT == ASR_BF16 ? 2 : 4);
-    static constexpr int kGBytes = kTmaTile * (GT == ASR_BF16 ? 2 : 4);
-    static constexpr int kMBytes = kTmaTile * 4;
+    static constexpr int kTile = TmaShape<PT, GT>::kTile;
+    static constexpr int kPBytes = kTile * (PT == ASR_BF16 ? 2 : 4);
+    static constexpr int kGBytes = kTile * (GT == ASR_BF16 ? 2 : 4);
+    static constexpr int kMBytes = kTile * 4;
     static constexpr int kBytes = kPBytes + kGBytes + 2 * kMBytes;
     // as many stages as fit in the shared-memory budget, at most ASR_TMA_STAGES
     static constexpr int kFit = ASR_TMA_SMEM_KB * 1024 / kBytes;
     static constexpr int kStages = kFit < ASR_TMA_STAGES ? kFit : ASR_TMA_STAGES;
     static_assert(kStages >= 2, "need at least two stages");
-    static constexpr int kSmem = kStages * kBytes + 2 * kStages * 8 + kTmaConsumerWarps * 4;
+    static constexpr int kSmem = kStages * kBytes + 2 * kStages * 8 + TmaShape<PT, GT>::kWarps * 4;
 };
 
-// Locate tile `tile` of the table, advancing the cursor t.
+// Locate tile `tile` (of tile_elems elements) of the table, advancing the
+// cursor t.
 template <int CAP>
-__device__ __forceinline__ void find_tile(const AdamTable<CAP> &tab, uint64_t tile, int &t, uint64_t &off,
-                                          uint32_t &cnt)
+__device__ __forceinline__ void find_tile(const AdamTable<CAP> &tab, uint64_t tile, uint32_t tile_elems, int &t,
+                                          uint64_t &off, uint32_t &cnt)
 {
     while (tile >= tab.t[t].tile_end) ++t;
     const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
-    off = (tile - first) * static_cast<uint64_t>(kTmaTile);
+    off = (tile - first) * static_cast<uint64_t>(tile_elems);
     const uint64_t rest = tab.t[t].n - off;
-    cnt = rest < static_cast<uint64_t>(kTmaTile) ? static_cast<uint32_t>(rest) : static_cast<uint32_t>(kTmaTile);
+    cnt = rest < static_cast<uint64_t>(tile_elems) ? static_cast<uint32_t>(rest) : tile_elems;
 }
 
-// All tensors FAST (16-byte-aligned buffers, base % 4 == 0); tile size kTmaTile.
+// All tensors FAST (16-byte-aligned buffers, base % 4 == 0); tile and block
+// shape TmaShape<PT, GT>.
 template <int PT, int GT, int RM, int CAP>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
 adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P,
                     uint64_t limit_ns)
 {
     using S = TmaStage<PT, GT>;
+    using SH = TmaShape<PT, GT>;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
     const uint32_t bars = sbase + S::kStages * S::kBytes;      // full[s] then empty[s]
@@ -209,14 +213,14 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), kTmaConsumerWarps);
+            mbar_init(empty(s), SH::kWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kTmaConsumerWarps) {
+    if (warp == SH::kWarps) {
         // ------------------------------------------------------ producer
         if (lane != 0) return;
         uint64_t policy;
@@ -229,7 +233,7 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
             if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
             uint64_t off;
             uint32_t cnt;
-            find_tile(tab, tile, t, off, cnt);
+            find_tile(tab, tile, S::kTile, t, off, cnt);
             const TensorEntry &T = tab.t[t];
             const uint32_t c8 = cnt & ~7u;
             const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
@@ -257,7 +261,7 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
     }
 
     // ---------------------------------------------------------- consumers
-    const int ct = threadIdx.x;            // 0 .. kTmaConsumers-1
+    const int ct = threadIdx.x;            // 0 .. SH::kConsumers-1
     const uint32_t dep_slot = bars + 16u * S::kStages + 4u * warp;   // one word per consumer warp
     int t = 0;
     uint32_t k = 0;
@@ -267,14 +271,14 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
         if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
         uint64_t off;
         uint32_t cnt;
-        find_tile(tab, tile, t, off, cnt);
+        find_tile(tab, tile, S::kTile, t, off, cnt);
         const TensorEntry &T = tab.t[t];
         const uint32_t c8 = cnt & ~7u;
         const unsigned char *st = smem + s * S::kBytes;
-        VecUnit<PT, GT> u[kTmaUnits];
+        VecUnit<PT, GT> u[SH::kUnits];
 #pragma unroll
-        for (int j = 0; j < kTmaUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+        for (int j = 0; j < SH::kUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
             if (e < c8) {
                 if (PT == ASR_BF16) {
                     const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 2);
@@ -312,8 +316,8 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
         // every folded load is back.
         uint32_t dep = 0;
 #pragma unroll
-        for (int j = 0; j < kTmaUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+        for (int j = 0; j < SH::kUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
             if (e < c8)
                 dep ^= u[j].p[0] ^ u[j].g[0] ^ __float_as_uint(u[j].m[0]) ^ __float_as_uint(u[j].m[4]) ^
                        __float_as_uint(u[j].v[0]) ^ __float_as_uint(u[j].v[4]) ^
@@ -326,11 +330,11 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
             mbar_arrive(empty(s));
         }
 #pragma unroll
-        for (int j = 0; j < kTmaUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+        for (int j = 0; j < SH::kUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
             if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
         }
         // a ragged end of a tensor (< 8 elements) goes through the scalar path
-        if (c8 < cnt && ct == (c8 / kVec) % kTmaConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
+        if (c8 < cnt && ct == (c8 / kVec) % SH::kConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
     }
 }

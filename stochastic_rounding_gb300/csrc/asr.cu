@@ -169,7 +169,7 @@ bool desc_fast(const asr_tensor_desc &d)
 // Dynamic shared memory opt-in and persistent grid of the bulk-copy kernel,
 // cached per (device, kernel).
 template <typename K>
-asr_status tma_grid(K kernel, int smem, int *grid)
+asr_status tma_grid(K kernel, int threads, int smem, int *grid)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -188,7 +188,7 @@ asr_status tma_grid(K kernel, int smem, int *grid)
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kTmaThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
     if (e != cudaSuccess) return cuda_fail(e);
     if (per_sm < 1) per_sm = 1;
     *grid = sms * per_sm;
@@ -202,7 +202,7 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
 {
     static_assert(CAP >= 1, "");
     constexpr bool kTma = FAST && ASR_USE_TMA;
-    constexpr uint64_t tile = kTma ? kTmaTile : kTile;
+    constexpr uint64_t tile = kTma ? TmaShape<PT, GT>::kTile : kTile;
     AdamTable<CAP> tab;
     std::memset(&tab, 0, sizeof(tab));
     uint64_t tiles = 0;
@@ -226,10 +226,10 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
     if (kTma) {
         auto kernel = adamw_sr_tma_kernel<PT, GT, RM, CAP>;
         const int smem = TmaStage<PT, GT>::kSmem;
-        st = tma_grid(kernel, smem, &grid);
+        st = tma_grid(kernel, TmaShape<PT, GT>::kThreads, smem, &grid);
         if (st != ASR_OK) return st;
         if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
-        kernel<<<grid, kTmaThreads, smem, stream>>>(tab, P, kWaitLimitNs);
+        kernel<<<grid, TmaShape<PT, GT>::kThreads, smem, stream>>>(tab, P, kWaitLimitNs);
     } else {
         auto kernel = adamw_sr_kernel<PT, GT, RM, FAST, CAP>;
         st = persistent_grid(kernel, &grid);

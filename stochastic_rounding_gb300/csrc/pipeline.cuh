@@ -20,24 +20,41 @@
 #ifndef ASR_TMA_STAGES
 #define ASR_TMA_STAGES 4
 #endif
-#ifndef ASR_TMA_CONSUMER_WARPS
-#define ASR_TMA_CONSUMER_WARPS 20
-#endif
 #ifndef ASR_TMA_SMEM_KB
 #define ASR_TMA_SMEM_KB 200
 #endif
 #ifndef ASR_TMA_EVICT_FIRST
 #define ASR_TMA_EVICT_FIRST 1
 #endif
-#ifndef ASR_TMA_TILE
-#define ASR_TMA_TILE 5120
+
+// Pipeline shape per (param, grad) dtype: the number of consumer warps, one
+// 8-element unit per consumer thread per tile.  Measured on GB300, one
+// 268M-element tensor per combination, all shapes in the same run (GB/s):
+//   bf16/bf16: 20 warps 6,538 (16: 6,232; 12: 5,204) -- the most arithmetic
+//              per byte (Philox and rounding), so the most warps;
+//   bf16/f32:  16 warps 6,669 (20: 6,601; 12: 5,613);
+//   f32/bf16:  12 warps 6,341 (20: 6,079; 16: 6,072);
+//   f32/f32:   12 warps 6,667 (20: 6,071; 16: 6,065) -- with 48 KB tiles
+//              four stages fit where 80 KB tiles allowed two.
+template <int PT, int GT>
+struct TmaShape {
+#ifdef ASR_TMA_WARPS
+    static constexpr int kWarps = ASR_TMA_WARPS;            // one shape for all, for sweeps
+#else
+    static constexpr int kWarps = PT == ASR_BF16 ? (GT == ASR_BF16 ? 20 : 16) : 12;
 #endif
-constexpr int kTmaTile = ASR_TMA_TILE;
-constexpr int kTmaConsumerWarps = ASR_TMA_CONSUMER_WARPS;
-constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
-constexpr int kTmaThreads = kTmaConsumers + 32;        // + one producer warp
-constexpr int kTmaUnits = kTmaTile / kVec / kTmaConsumers;   // units per consumer thread per tile
-static_assert(kTmaUnits >= 1 && kTmaUnits * kTmaConsumers * kVec == kTmaTile, "tile must split evenly");
+    static constexpr int kConsumers = kWarps * 32;
+    static constexpr int kThreads = kConsumers + 32;        // + one producer warp
+    static constexpr int kUnits = 1;                        // 8-element units per consumer thread per tile
+    static constexpr int kTile = kConsumers * kVec * kUnits;
+};
+
+inline int tma_tile(int pdt, int gdt)
+{
+    if (pdt == ASR_BF16) return gdt == ASR_BF16 ? TmaShape<ASR_BF16, ASR_BF16>::kTile : TmaShape<ASR_BF16, ASR_F32>::kTile;
+    return gdt == ASR_BF16 ? TmaShape<ASR_F32, ASR_BF16>::kTile : TmaShape<ASR_F32, ASR_F32>::kTile;
+}
+
 constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: a healthy wait takes microseconds
 
 constexpr uint32_t kErrWaitTimeout = 1u;

@@ -22,23 +22,24 @@ struct GlobalTable {
     uint64_t total_tiles;
 };
 
-__device__ __forceinline__ void find_tile(const GlobalTable &tab, uint64_t tile, int &t, uint64_t &off,
-                                          uint32_t &cnt)
+__device__ __forceinline__ void find_tile(const GlobalTable &tab, uint64_t tile, uint32_t tile_elems, int &t,
+                                          uint64_t &off, uint32_t &cnt)
 {
     while (tile >= tab.t[t].tile_end) ++t;
     const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
-    off = (tile - first) * static_cast<uint64_t>(kTmaTile);
+    off = (tile - first) * static_cast<uint64_t>(tile_elems);
     const uint64_t rest = tab.t[t].n - off;
-    cnt = rest < static_cast<uint64_t>(kTmaTile) ? static_cast<uint32_t>(rest) : static_cast<uint32_t>(kTmaTile);
+    cnt = rest < static_cast<uint64_t>(tile_elems) ? static_cast<uint32_t>(rest) : tile_elems;
 }
 
 // The pipeline of adamw_sr_tma_kernel, with the table read from global memory.
 template <int PT, int GT, int RM>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
 adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid_constant__ AdamParams P,
                            uint64_t limit_ns)
 {
     using S = TmaStage<PT, GT>;
+    using SH = TmaShape<PT, GT>;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
     const uint32_t bars = sbase + S::kStages * S::kBytes;
@@ -48,14 +49,14 @@ adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), kTmaConsumerWarps);
+            mbar_init(empty(s), SH::kWarps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kTmaConsumerWarps) {
+    if (warp == SH::kWarps) {
         if (lane != 0) return;
         uint64_t policy;
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
@@ -67,7 +68,7 @@ adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid
             if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
             uint64_t off;
             uint32_t cnt;
-            find_tile(tab, tile, t, off, cnt);
+            find_tile(tab, tile, S::kTile, t, off, cnt);
             const TensorEntry &T = tab.t[t];
             const uint32_t c8 = cnt & ~7u;
             const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
@@ -103,15 +104,15 @@ adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid
         if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
         uint64_t off;
         uint32_t cnt;
-        find_tile(tab, tile, t, off, cnt);
+        find_tile(tab, tile, S::kTile, t, off, cnt);
         const TensorEntry &T = tab.t[t];
         const uint32_t c8 = cnt & ~7u;
         const unsigned char *st = smem + s * S::kBytes;
-        VecUnit<PT, GT> u[kTmaUnits];
+        VecUnit<PT, GT> u[SH::kUnits];
         uint32_t dep = 0;
 #pragma unroll
-        for (int j = 0; j < kTmaUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+        for (int j = 0; j < SH::kUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
             if (e < c8) {
                 if (PT == ASR_BF16) {
                     const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 2);
@@ -152,11 +153,11 @@ adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid
             mbar_arrive(empty(s));
         }
 #pragma unroll
-        for (int j = 0; j < kTmaUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * kTmaConsumers + ct) * kVec;
+        for (int j = 0; j < SH::kUnits; ++j) {
+            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
             if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
         }
-        if (c8 < cnt && ct == (c8 / kVec) % kTmaConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
+        if (c8 < cnt && ct == (c8 / kVec) % SH::kConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
     }
 }
 
@@ -220,13 +221,13 @@ asr_status launch_static_group(int dev, const TensorEntry *dev_table, uint64_t t
     auto kernel = adamw_sr_tma_static_kernel<PT, GT, RM>;
     const int smem = TmaStage<PT, GT>::kSmem;
     int grid = 0;
-    asr_status st = static_grid(kernel, dev, variant_slot(PT, GT, RM), kTmaThreads, smem, &grid);
+    asr_status st = static_grid(kernel, dev, variant_slot(PT, GT, RM), TmaShape<PT, GT>::kThreads, smem, &grid);
     if (st != ASR_OK) return st;
     if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
     GlobalTable tab;
     tab.t = dev_table;
     tab.total_tiles = tiles;
-    kernel<<<grid, kTmaThreads, smem, stream>>>(tab, P, kWaitLimitNs);
+    kernel<<<grid, TmaShape<PT, GT>::kThreads, smem, stream>>>(tab, P, kWaitLimitNs);
     return check_launch();
 }
 
@@ -323,7 +324,7 @@ asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, con
             T.v = d.exp_avg_sq;
             T.n = d.n;
             T.base = d.base_index;
-            tiles += (d.n + kTmaTile - 1) / kTmaTile;
+            tiles += (d.n + tma_tile(pdt, gdt) - 1) / tma_tile(pdt, gdt);
             T.tile_end = tiles;
         }
         group_count[gi] = used - group_start[gi];
