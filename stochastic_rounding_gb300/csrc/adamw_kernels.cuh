@@ -182,10 +182,11 @@ struct TmaStage {
     static constexpr int kSmem = kStages * kBytes + 2 * kStages * 8 + TmaShape<PT, GT>::kWarps * 4;
 };
 
-// Locate tile `tile` (of tile_elems elements) of the table, advancing the
-// cursor t.
-template <int CAP>
-__device__ __forceinline__ void find_tile(const AdamTable<CAP> &tab, uint64_t tile, uint32_t tile_elems, int &t,
+// Locate tile `tile` (of tile_elems elements) of a descriptor table, advancing
+// the cursor t.  Tab is AdamTable<CAP> (descriptors in the launch parameters)
+// or any type with the same `t[]` and `total_tiles` members.
+template <typename Tab>
+__device__ __forceinline__ void find_tile(const Tab &tab, uint64_t tile, uint32_t tile_elems, int &t,
                                           uint64_t &off, uint32_t &cnt)
 {
     while (tile >= tab.t[t].tile_end) ++t;
@@ -195,12 +196,11 @@ __device__ __forceinline__ void find_tile(const AdamTable<CAP> &tab, uint64_t ti
     cnt = rest < static_cast<uint64_t>(tile_elems) ? static_cast<uint32_t>(rest) : tile_elems;
 }
 
-// All tensors FAST (16-byte-aligned buffers, base % 4 == 0); tile and block
-// shape TmaShape<PT, GT>.
-template <int PT, int GT, int RM, int CAP>
-__global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
-adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P,
-                    uint64_t limit_ns)
+// The body of the pipelined step, shared by the kernels that differ only in
+// where their descriptor table lives.  All tensors FAST (16-byte-aligned
+// buffers, base % 4 == 0); tile and block shape TmaShape<PT, GT>.
+template <int PT, int GT, int RM, typename Tab>
+__device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, uint64_t limit_ns)
 {
     using S = TmaStage<PT, GT>;
     using SH = TmaShape<PT, GT>;
@@ -337,4 +337,13 @@ adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_con
         // a ragged end of a tensor (< 8 elements) goes through the scalar path
         if (c8 < cnt && ct == (c8 / kVec) % SH::kConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
     }
+}
+
+// Descriptor table in the launch parameters (up to CAP tensors).
+template <int PT, int GT, int RM, int CAP>
+__global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
+adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P,
+                    uint64_t limit_ns)
+{
+    tma_step<PT, GT, RM>(tab, P, limit_ns);
 }

@@ -41,6 +41,10 @@
 
 namespace gemm {
 
+#ifndef ASR_GEMM_PAIR
+#define ASR_GEMM_PAIR 1            // 1: two-SM (CTA pair) kernel where pairs fit; 0: one-SM kernel only
+#endif
+
 constexpr int kBM = 128;                   // tile rows (M) = TMEM lanes
 constexpr int kBN = 256;                   // tile columns (N) = TMEM columns
 constexpr int kBK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
@@ -120,14 +124,53 @@ struct GemmParams {
     RoundKeys keys;
 };
 
-// Tile t of the grouped order: groups of kGroupM M-tiles, walked column by
+// Epilogue of one warp: accumulator row `row` of the output (this lane's
+// TMEM lane, columns from tq), columns n0 .. n0+ncols-1, rounded to bf16
+// (stochastic or nearest-even) and stored, with the f32 accumulator if asked
+// for.  tcgen05.ld is warp-collective, so every lane loads, and lanes whose
+// row lies past M (zeros read past the edge) store nothing.
+__device__ __forceinline__ void store_rows(const GemmParams &P, uint32_t tq, uint32_t row, uint32_t n0, int ncols)
+{
+    for (int c = 0; c < ncols; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tq + c, v);
+        if (row >= P.m) continue;
+        const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
+        uint32_t w[8];
+        if (P.rounding == ASR_ROUND_SR) {
+            uint32_t r[16];
+            philox_q(e0 >> 2, P.step, P.keys, r);
+            philox_q((e0 >> 2) + 1, P.step, P.keys, r + 4);
+            philox_q((e0 >> 2) + 2, P.step, P.keys, r + 8);
+            philox_q((e0 >> 2) + 3, P.step, P.keys, r + 12);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                w[k] = sr_pack2<true>(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), r[2 * k],
+                                      r[2 * k + 1]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                w[k] = pack_bf16(round_rne(__uint_as_float(v[2 * k])), round_rne(__uint_as_float(v[2 * k + 1])));
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (P.c_f32) {
+            uint4 *df = reinterpret_cast<uint4 *>(P.c_f32 + e0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) df[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+    }
+}
+
+// Tile t of the grouped order: groups of `group` M-tiles, walked column by
 // column across N (M fastest inside a group).
 __device__ __forceinline__ void tile_coords(uint32_t t, uint32_t tiles_m, uint32_t tiles_n, uint32_t &mt,
-                                            uint32_t &nt)
+                                            uint32_t &nt, uint32_t group = kGroupM)
 {
-    const uint32_t group_size = kGroupM * tiles_n;
-    const uint32_t first_m = (t / group_size) * kGroupM;
-    const uint32_t gm = tiles_m - first_m < static_cast<uint32_t>(kGroupM) ? tiles_m - first_m : kGroupM;
+    const uint32_t group_size = group * tiles_n;
+    const uint32_t first_m = (t / group_size) * group;
+    const uint32_t gm = tiles_m - first_m < group ? tiles_m - first_m : group;
     const uint32_t local = t % group_size;
     mt = first_m + local % gm;
     nt = local / gm;
@@ -244,38 +287,7 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
             const uint32_t n0 = nt * kBN;
             const uint32_t tq = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * kBN);
             const int ncols = static_cast<int>(P.n - n0) < kBN ? static_cast<int>(P.n - n0) : kBN;
-            for (int c = 0; c < ncols; c += 16) {
-                uint32_t v[16];
-                tmem_ld16(tq + c, v);               // warp-collective: every lane loads
-                if (row >= P.m) continue;           // rows past M (zeros read past the edge) are not stored
-                const uint64_t e0 = static_cast<uint64_t>(row) * P.n + n0 + c;   // multiple of 16
-                uint32_t w[8];
-                if (P.rounding == ASR_ROUND_SR) {
-                    uint32_t r[16];
-                    philox_q(e0 >> 2, P.step, P.keys, r);
-                    philox_q((e0 >> 2) + 1, P.step, P.keys, r + 4);
-                    philox_q((e0 >> 2) + 2, P.step, P.keys, r + 8);
-                    philox_q((e0 >> 2) + 3, P.step, P.keys, r + 12);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        w[k] = sr_pack2<true>(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), r[2 * k],
-                                              r[2 * k + 1]);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        w[k] = pack_bf16(round_rne(__uint_as_float(v[2 * k])),
-                                         round_rne(__uint_as_float(v[2 * k + 1])));
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                if (P.c_f32) {
-                    uint4 *df = reinterpret_cast<uint4 *>(P.c_f32 + e0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        df[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
-            }
+            store_rows(P, tq, row, n0, ncols);
             // this warp is done reading accumulator b
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
@@ -289,6 +301,268 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
         __syncwarp();
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ----------------------------------------------------- two-SM (CTA pair) form
+//
+// The same product with 256 x 256 tiles computed by a cluster of two CTAs on
+// neighbouring SMs with tcgen05.mma.cta_group::2: each CTA stages its own 128
+// rows of A and its own 128 rows (of N) of B, and one M=256, N=256 MMA
+// issued by the pair's first CTA reads all four halves, leaving rows
+// 0..127 of the tile in the first CTA's tensor memory and rows 128..255 in
+// the second's, all 256 columns each.  Per FLOP every SM stages and reads a
+// third less shared memory than with 128 x 256 tiles on one SM.
+//   both CTAs, warp 0 lane 0: stream the CTA's halves of A and B into a
+//       6-stage ring; the bytes of both CTAs are counted on the FIRST CTA's
+//       "full" barrier (.cta_group::2 bulk tensor copies may signal the
+//       peer's barrier), which its producer arms with both CTAs' bytes;
+//   both CTAs, warp 1: allocate / free the tensor memory as a pair; in the
+//       first CTA its lane 0 issues the MMAs and commits them, multicast to
+//       both CTAs: each slice to the "empty" barrier of its stage (both
+//       producers wait on their own), each tile to both "acc_full" barriers;
+//   both CTAs, warps 2..5: the epilogue of the CTA's 128 rows; each warp
+//       hands the accumulator back by arriving on the FIRST CTA's acc_empty
+//       barrier (eight arrivals per tile).
+// A slice whose rows lie wholly past M (or N) in the second half of a tile
+// is read from row 0 instead: its products land only in rows (columns) the
+// epilogue never stores, and no copy starts outside the matrix.
+constexpr int kPairBM = 256;                // pair tile rows: 128 per CTA
+constexpr int kPairBN = 256;                // pair tile columns: B rows, 128 staged per CTA
+constexpr int kPairStages = 6;
+constexpr int kPairGroupM = 8;
+constexpr uint32_t kHalfA = 128 * kBK * 2;          // 16 KB per CTA
+constexpr uint32_t kHalfB = 128 * kBK * 2;          // 16 KB per CTA
+constexpr uint32_t kPairStageBytes = kHalfA + kHalfB;
+// barriers: full/empty per stage, full/empty per accumulator, the MMA drain
+constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + (2 * kPairStages + 2 * kAccBufs + 1) * 8 + 16;
+constexpr uint32_t kPairInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kPairBN >> 3) << 17) |
+                                    (uint32_t(kPairBM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// An mbarrier wait that also orders what the other CTA of the cluster did
+// before arriving (acquire at cluster scope); bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t polls = 0; !mbar_test_cluster(bar, parity); ++polls) {
+        if (global_ns() - t0 > limit_ns || polls >= kWaitMaxPolls) {
+            atomicOr(&g_device_error, kErrWaitTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
+                                                 uint32_t cluster_bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kPairInstrDesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on the barrier at this offset in both CTAs of the pair when
+// every MMA issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar)
+{
+    const uint16_t both = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"(both)
+        : "memory");
+}
+
+// Persistent over pair tiles: cluster c walks tiles c, c + clusters, ...
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                         const __grid_constant__ GemmParams P, uint64_t limit_ns)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;          // same offset in both CTAs
+    const uint32_t bars = base + kPairStages * kPairStageBytes;
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto empty = [&](int s) { return bars + 8u * (kPairStages + s); };
+    auto acc_full = [&](int b) { return bars + 8u * (2 * kPairStages + b); };
+    auto acc_empty = [&](int b) { return bars + 8u * (2 * kPairStages + kAccBufs + b); };
+    const uint32_t drained = bars + 8u * (2 * kPairStages + 2 * kAccBufs);
+    const uint32_t tmem_slot = drained + 8u;
+    const uint32_t *tmem_slot_ptr = reinterpret_cast<const uint32_t *>(smem_raw + (tmem_slot - raw));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const uint32_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+    const uint32_t tiles_m = (P.m + kPairBM - 1) / kPairBM, tiles_n = (P.n + kPairBN - 1) / kPairBN;
+    const uint32_t tiles = tiles_m * tiles_n;
+    const int kblocks = static_cast<int>((P.k + kBK - 1) / kBK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), 2 * kEpilogueWarps);
+        }
+        mbar_init(drained, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    }
+    // both CTAs' barriers are initialised before either CTA signals the other's
+    cluster_sync();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot_ptr;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------- producer
+        uint32_t g = 0;
+        bool ok = true;
+        for (uint32_t t = cluster; ok && t < tiles; t += clusters) {
+            uint32_t mt, nt;
+            tile_coords(t, tiles_m, tiles_n, mt, nt, kPairGroupM);
+            uint32_t ra = mt * kPairBM + rank * 128, rb = nt * kPairBN + rank * 128;
+            if (ra >= P.m) ra = 0;
+            if (rb >= P.n) rb = 0;
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                const int s = static_cast<int>(g % kPairStages);
+                const uint32_t use = g / kPairStages;
+                if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) mbar_arrive_expect_tx(full(s), 2 * kPairStageBytes);
+                const uint32_t bar = peer_addr(full(s), 0);
+                const uint32_t dst = base + s * kPairStageBytes;
+                tma_load_2d_pair(dst, &map_a, kb * kBK, static_cast<int32_t>(ra), bar);
+                tma_load_2d_pair(dst + kHalfA, &map_b, kb * kBK, static_cast<int32_t>(rb), bar);
+            }
+        }
+        // the MMAs that read this CTA's stages have completed, and their
+        // arrivals on its barriers have landed, before the CTA exits
+        for (uint32_t s = 0; s < static_cast<uint32_t>(kPairStages) && s < g; ++s) {
+            const uint32_t last_use = (g - 1 - s) / kPairStages;
+            mbar_wait(empty(static_cast<int>(s)), last_use & 1u, limit_ns);
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------------ MMA issuer
+        uint32_t g = 0, i = 0;
+        bool ok = true;
+        for (uint32_t t = cluster; ok && t < tiles; t += clusters, ++i) {
+            const int b = static_cast<int>(i % kAccBufs);
+            const uint32_t ub = i / kAccBufs;
+            if (ub > 0 && !mbar_wait_cluster(acc_empty(b), (ub - 1) & 1u, limit_ns)) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t d = tmem + static_cast<uint32_t>(b * kPairBN);
+            for (int kb = 0; kb < kblocks; ++kb, ++g) {
+                const int s = static_cast<int>(g % kPairStages);
+                const uint32_t use = g / kPairStages;
+                if (!mbar_wait(full(s), use & 1u, limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t sa = base + s * kPairStageBytes, sb = sa + kHalfA;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_bf16_pair(d, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), (kb | kk) != 0);
+                mma_commit_pair(empty(s));
+            }
+            mma_commit_pair(acc_full(b));
+        }
+        // every MMA issued here has completed before the pair may free its
+        // tensor memory or leave (also after a timeout)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(drained)
+                     : "memory");
+        mbar_wait(drained, 0, limit_ns);
+    } else if (warp >= 2) {
+        // ------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        uint32_t i = 0;
+        for (uint32_t t = cluster; t < tiles; t += clusters, ++i) {
+            const int b = static_cast<int>(i % kAccBufs);
+            const uint32_t ub = i / kAccBufs;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(b), ub & 1u, limit_ns))) break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            uint32_t mt, nt;
+            tile_coords(t, tiles_m, tiles_n, mt, nt, kPairGroupM);
+            const uint32_t row = mt * kPairBM + rank * 128 + quarter * 32 + lane;
+            const uint32_t n0 = nt * kPairBN;
+            const uint32_t tq =
+                tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * kPairBN);
+            const int ncols = static_cast<int>(P.n - n0) < kPairBN ? static_cast<int>(P.n - n0) : kPairBN;
+            store_rows(P, tq, row, n0, ncols);
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(peer_addr(acc_empty(b), 0));
+        }
+    }
+    // ------------------------------------------------------------ cleanup
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncwarp();
+    cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -313,22 +587,49 @@ asr_status encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
     return ASR_OK;
 }
 
-// The kernel's dynamic shared memory is above the default 48 KB: opt in once
-// per device.
-bool g_smem_opted[kMaxDevices];
+// Per device, once: opt both kernels in to their dynamic shared memory
+// (above the default 48 KB) and find how many CTA pairs of the two-SM kernel
+// can be resident at once (pairs sit on neighbouring SMs, so on a GPU with an
+// odd number of SMs somewhere fewer than SMs/2 fit).
+bool g_gemm_ready[kMaxDevices];
+int g_gemm_sms[kMaxDevices];
+int g_gemm_pairs[kMaxDevices];
 
-asr_status smem_opt_in()
+asr_status device_setup(int *sms, int *pairs)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return ASR_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lk(g_encode_mu);
-    if (!g_smem_opted[dev]) {
+    if (!g_gemm_ready[dev]) {
         e = cudaFuncSetAttribute(gemm_bf16_sr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_bf16_sr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPairSmem);
+        int n_sms = 0, n_pairs = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(n_sms & ~1), 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = kPairSmem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&n_pairs, gemm_bf16_sr_pair_kernel, &cfg);
+        }
         if (e != cudaSuccess) return cuda_fail(e);
-        g_smem_opted[dev] = true;
+        g_gemm_sms[dev] = n_sms;
+        g_gemm_pairs[dev] = n_pairs;
+        g_gemm_ready[dev] = true;
     }
+    *sms = g_gemm_sms[dev];
+    *pairs = g_gemm_pairs[dev];
     return ASR_OK;
 }
 
@@ -358,12 +659,8 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (m > (1u << 24) || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
         return ASR_ERR_INVALID_VALUE;
-    CUtensorMap ma, mb;
-    asr_status st = make_map(&ma, a, m, k, kBM);
-    if (st != ASR_OK) return st;
-    st = make_map(&mb, b, n, k, kBN);
-    if (st != ASR_OK) return st;
-    st = smem_opt_in();
+    int sms = 0, pairs = 0;
+    asr_status st = device_setup(&sms, &pairs);
     if (st != ASR_OK) return st;
     GemmParams P;
     P.c = c;
@@ -374,10 +671,37 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     P.step = step;
     P.rounding = rounding;
     P.keys = make_keys(seed);
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e);
+    CUtensorMap ma, mb;
+#if ASR_GEMM_PAIR
+    if (pairs > 0) {
+        // two-SM form: both operands in 128-row boxes (one half per CTA)
+        st = make_map(&ma, a, m, k, 128);
+        if (st == ASR_OK) st = make_map(&mb, b, n, k, 128);
+        if (st != ASR_OK) return st;
+        const uint64_t tiles = ((m + kPairBM - 1) / kPairBM) * ((n + kPairBN - 1) / kPairBN);
+        if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
+        const unsigned clusters = static_cast<unsigned>(tiles < static_cast<uint64_t>(pairs) ? tiles : pairs);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * clusters, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPairSmem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const uint64_t limit = kWaitLimitNs;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel, ma, mb, P, limit);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return check_launch();
+    }
+#endif
+    st = make_map(&ma, a, m, k, kBM);
+    if (st == ASR_OK) st = make_map(&mb, b, n, k, kBN);
+    if (st != ASR_OK) return st;
     const uint64_t tiles = ((m + kBM - 1) / kBM) * ((n + kBN - 1) / kBN);
     if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
     const unsigned grid = static_cast<unsigned>(tiles < static_cast<uint64_t>(sms) ? tiles : sms);

@@ -22,143 +22,13 @@ struct GlobalTable {
     uint64_t total_tiles;
 };
 
-__device__ __forceinline__ void find_tile(const GlobalTable &tab, uint64_t tile, uint32_t tile_elems, int &t,
-                                          uint64_t &off, uint32_t &cnt)
-{
-    while (tile >= tab.t[t].tile_end) ++t;
-    const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
-    off = (tile - first) * static_cast<uint64_t>(tile_elems);
-    const uint64_t rest = tab.t[t].n - off;
-    cnt = rest < static_cast<uint64_t>(tile_elems) ? static_cast<uint32_t>(rest) : tile_elems;
-}
-
-// The pipeline of adamw_sr_tma_kernel, with the table read from global memory.
+// The pipelined step with its table read from global memory (g_static_table).
 template <int PT, int GT, int RM>
 __global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
 adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid_constant__ AdamParams P,
                            uint64_t limit_ns)
 {
-    using S = TmaStage<PT, GT>;
-    using SH = TmaShape<PT, GT>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const uint32_t sbase = smem_addr(smem);
-    const uint32_t bars = sbase + S::kStages * S::kBytes;
-    auto full = [&](int s) { return bars + 8u * s; };
-    auto empty = [&](int s) { return bars + 8u * (S::kStages + s); };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), SH::kWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == SH::kWarps) {
-        if (lane != 0) return;
-        uint64_t policy;
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-        int t = 0;
-        uint32_t k = 0;
-        for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
-            const int s = static_cast<int>(k % S::kStages);
-            const uint32_t use = k / S::kStages;
-            if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
-            uint64_t off;
-            uint32_t cnt;
-            find_tile(tab, tile, S::kTile, t, off, cnt);
-            const TensorEntry &T = tab.t[t];
-            const uint32_t c8 = cnt & ~7u;
-            const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
-            const uint32_t mb = c8 * 4u;
-            mbar_arrive_expect_tx(full(s), pb + gb + 2 * mb);
-            if (c8) {
-                const uint32_t dst = sbase + s * S::kBytes;
-                bulk_load(dst, static_cast<const unsigned char *>(T.p) + off * (PT == ASR_BF16 ? 2 : 4), pb,
-                          full(s), policy);
-                bulk_load(dst + S::kPBytes, static_cast<const unsigned char *>(T.g) + off * (GT == ASR_BF16 ? 2 : 4),
-                          gb, full(s), policy);
-                bulk_load(dst + S::kPBytes + S::kGBytes, T.m + off, mb, full(s), policy);
-                bulk_load(dst + S::kPBytes + S::kGBytes + S::kMBytes, T.v + off, mb, full(s), policy);
-            }
-        }
-        // every copy issued here must land before the CTA exits
-        const uint32_t issued = k;
-        for (int s = 0; s < S::kStages; ++s) {
-            if (static_cast<uint32_t>(s) >= issued) break;
-            const uint32_t last_use = (issued - 1 - s) / S::kStages;
-            mbar_wait(full(s), last_use & 1u, limit_ns);
-        }
-        return;
-    }
-
-    const int ct = threadIdx.x;
-    const uint32_t dep_slot = bars + 16u * S::kStages + 4u * warp;
-    int t = 0;
-    uint32_t k = 0;
-    for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
-        const int s = static_cast<int>(k % S::kStages);
-        const uint32_t use = k / S::kStages;
-        if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
-        uint64_t off;
-        uint32_t cnt;
-        find_tile(tab, tile, S::kTile, t, off, cnt);
-        const TensorEntry &T = tab.t[t];
-        const uint32_t c8 = cnt & ~7u;
-        const unsigned char *st = smem + s * S::kBytes;
-        VecUnit<PT, GT> u[SH::kUnits];
-        uint32_t dep = 0;
-#pragma unroll
-        for (int j = 0; j < SH::kUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
-            if (e < c8) {
-                if (PT == ASR_BF16) {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 2);
-                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
-                } else {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(st + e * 4);
-                    const uint4 b = *reinterpret_cast<const uint4 *>(st + e * 4 + 16);
-                    u[j].p[0] = a.x; u[j].p[1] = a.y; u[j].p[2] = a.z; u[j].p[3] = a.w;
-                    u[j].p[4] = b.x; u[j].p[5] = b.y; u[j].p[6] = b.z; u[j].p[7] = b.w;
-                }
-                const unsigned char *gs = st + S::kPBytes;
-                if (GT == ASR_BF16) {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 2);
-                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
-                } else {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(gs + e * 4);
-                    const uint4 b = *reinterpret_cast<const uint4 *>(gs + e * 4 + 16);
-                    u[j].g[0] = a.x; u[j].g[1] = a.y; u[j].g[2] = a.z; u[j].g[3] = a.w;
-                    u[j].g[4] = b.x; u[j].g[5] = b.y; u[j].g[6] = b.z; u[j].g[7] = b.w;
-                }
-                const float4 *ms = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + e * 4);
-                const float4 *vs = reinterpret_cast<const float4 *>(st + S::kPBytes + S::kGBytes + S::kMBytes + e * 4);
-                const float4 m0 = ms[0], m1 = ms[1], v0 = vs[0], v1 = vs[1];
-                u[j].m[0] = m0.x; u[j].m[1] = m0.y; u[j].m[2] = m0.z; u[j].m[3] = m0.w;
-                u[j].m[4] = m1.x; u[j].m[5] = m1.y; u[j].m[6] = m1.z; u[j].m[7] = m1.w;
-                u[j].v[0] = v0.x; u[j].v[1] = v0.y; u[j].v[2] = v0.z; u[j].v[3] = v0.w;
-                u[j].v[4] = v1.x; u[j].v[5] = v1.y; u[j].v[6] = v1.z; u[j].v[7] = v1.w;
-                dep ^= u[j].p[0] ^ u[j].g[0] ^ __float_as_uint(m0.x) ^ __float_as_uint(m1.x) ^
-                       __float_as_uint(v0.x) ^ __float_as_uint(v1.x) ^ (PT == ASR_BF16 ? 0u : u[j].p[4]) ^
-                       (GT == ASR_BF16 ? 0u : u[j].g[4]);
-            }
-        }
-        // release the stage only after this warp's loads have returned
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(dep_slot), "r"(dep) : "memory");
-        __syncwarp();
-        if (lane == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(empty(s));
-        }
-#pragma unroll
-        for (int j = 0; j < SH::kUnits; ++j) {
-            const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
-            if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
-        }
-        if (c8 < cnt && ct == (c8 / kVec) % SH::kConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
-    }
+    tma_step<PT, GT, RM>(tab, P, limit_ns);
 }
 
 // Per-device set-up of this path, kept in fixed arrays (no allocation): the
