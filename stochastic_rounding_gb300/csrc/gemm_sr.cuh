@@ -330,8 +330,14 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 // epilogue never stores, and no copy starts outside the matrix.
 constexpr int kPairBM = 256;                // pair tile rows: 128 per CTA
 constexpr int kPairBN = 256;                // pair tile columns: B rows, 128 staged per CTA
-constexpr int kPairStages = 6;
-constexpr int kPairGroupM = 8;
+#ifndef ASR_GEMM_PAIR_STAGES
+#define ASR_GEMM_PAIR_STAGES 6
+#endif
+#ifndef ASR_GEMM_PAIR_GROUP
+#define ASR_GEMM_PAIR_GROUP 8
+#endif
+constexpr int kPairStages = ASR_GEMM_PAIR_STAGES;   // 32 KB each: 6 fit beside the barriers, 7 just fit
+constexpr int kPairGroupM = ASR_GEMM_PAIR_GROUP;    // tile order: 8 pair-tile rows walked across N
 constexpr uint32_t kHalfA = 128 * kBK * 2;          // 16 KB per CTA
 constexpr uint32_t kHalfB = 128 * kBK * 2;          // 16 KB per CTA
 constexpr uint32_t kPairStageBytes = kHalfA + kHalfB;
