@@ -322,9 +322,9 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 //       first CTA its lane 0 issues the MMAs and commits them, multicast to
 //       both CTAs: each slice to the "empty" barrier of its stage (both
 //       producers wait on their own), each tile to both "acc_full" barriers;
-//   both CTAs, warps 2..5: the epilogue of the CTA's 128 rows; each warp
-//       hands the accumulator back by arriving on the FIRST CTA's acc_empty
-//       barrier (eight arrivals per tile).
+//   both CTAs, warps 2..5 (or 2..9): the epilogue of the CTA's 128 rows;
+//       each warp hands the accumulator back by arriving on the FIRST CTA's
+//       acc_empty barrier (2 x epilogue warps arrivals per tile).
 // A slice whose rows lie wholly past M (or N) in the second half of a tile
 // is read from row 0 instead: its products land only in rows (columns) the
 // epilogue never stores, and no copy starts outside the matrix.
@@ -336,6 +336,19 @@ constexpr int kPairBN = 256;                // pair tile columns: B rows, 128 st
 #ifndef ASR_GEMM_PAIR_GROUP
 #define ASR_GEMM_PAIR_GROUP 8
 #endif
+// Epilogue warps per CTA, a template parameter of the kernel: 4 (one per TMEM
+// lane quarter) or 8 (two per quarter, half of the columns each).  The
+// stochastic-rounding epilogue costs a Philox call per four outputs; below
+// K ~ 1,024 it takes longer than the tile's MMAs and 8 warps hide more of it.
+// Same-run TFLOP/s (4 / 8 warps): 8192^2 x 1024: 972-986 / 1,096-1,141;
+// 8192^2 x 2048: 1,472-1,501 / 1,408-1,455; 8192^3: 1,716-1,764 / 1,730-1,759.
+constexpr int kWideEpilogueMaxK = 1024;
+template <int EPI>
+struct PairShape {
+    static_assert(EPI == 4 || EPI == 8, "epilogue warps: 4 or 8");
+    static constexpr int kThreads = 64 + 32 * EPI;     // producer warp, MMA warp, epilogue
+    static constexpr int kSpan = 256 / (EPI / 4);      // columns per epilogue warp
+};
 constexpr int kPairStages = ASR_GEMM_PAIR_STAGES;   // 32 KB each: 6 fit beside the barriers, 7 just fit
 constexpr int kPairGroupM = ASR_GEMM_PAIR_GROUP;    // tile order: 8 pair-tile rows walked across N
 constexpr uint32_t kHalfA = 128 * kBK * 2;          // 16 KB per CTA
@@ -430,7 +443,8 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar)
 }
 
 // Persistent over pair tiles: cluster c walks tiles c, c + clusters, ...
-__global__ void __launch_bounds__(kThreads, 1)
+template <int EPI>
+__global__ void __launch_bounds__(PairShape<EPI>::kThreads, 1)
 gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                          const __grid_constant__ GemmParams P, uint64_t limit_ns)
 {
@@ -461,7 +475,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(acc_full(b), 1);
-            mbar_init(acc_empty(b), 2 * kEpilogueWarps);
+            mbar_init(acc_empty(b), 2 * EPI);
         }
         mbar_init(drained, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -541,7 +555,11 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         mbar_wait(drained, 0, limit_ns);
     } else if (warp >= 2) {
         // ------------------------------------------------------- epilogue
+        // a warp reads the TMEM lane quarter warp % 4; with 8 warps, two
+        // warps share a quarter and take half of the columns each
         const int quarter = warp & 3;
+        constexpr int kSpan = PairShape<EPI>::kSpan;
+        const int c_lo = ((warp - 2) / 4) * kSpan;
         uint32_t i = 0;
         for (uint32_t t = cluster; t < tiles; t += clusters, ++i) {
             const int b = static_cast<int>(i % kAccBufs);
@@ -555,7 +573,8 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             const uint32_t tq =
                 tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * kPairBN);
             const int ncols = static_cast<int>(P.n - n0) < kPairBN ? static_cast<int>(P.n - n0) : kPairBN;
-            store_rows(P, tq, row, n0, ncols);
+            const int c_hi = ncols < c_lo + kSpan ? ncols : c_lo + kSpan;
+            if (c_hi > c_lo) store_rows(P, tq + c_lo, row, n0 + c_lo, c_hi - c_lo);
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(peer_addr(acc_empty(b), 0));
@@ -599,9 +618,30 @@ asr_status encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
 // odd number of SMs somewhere fewer than SMs/2 fit).
 bool g_gemm_ready[kMaxDevices];
 int g_gemm_sms[kMaxDevices];
-int g_gemm_pairs[kMaxDevices];
+int g_gemm_pairs[kMaxDevices][2];
 
-asr_status device_setup(int *sms, int *pairs)
+template <int EPI>
+cudaError_t pair_setup(int n_sms, int *n_pairs)
+{
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_sr_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPairSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(n_sms & ~1), 1, 1);
+    cfg.blockDim = dim3(PairShape<EPI>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(n_pairs, gemm_bf16_sr_pair_kernel<EPI>, &cfg);
+}
+
+// pairs[0]: resident pairs of the 4-warp-epilogue kernel, pairs[1]: of the 8-warp one
+asr_status device_setup(int *sms, int pairs[2])
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -610,33 +650,43 @@ asr_status device_setup(int *sms, int *pairs)
     std::lock_guard<std::mutex> lk(g_encode_mu);
     if (!g_gemm_ready[dev]) {
         e = cudaFuncSetAttribute(gemm_bf16_sr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemm_bf16_sr_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kPairSmem);
-        int n_sms = 0, n_pairs = 0;
+        int n_sms = 0, p4 = 0, p8 = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(static_cast<unsigned>(n_sms & ~1), 1, 1);
-            cfg.blockDim = dim3(kThreads, 1, 1);
-            cfg.dynamicSmemBytes = kPairSmem;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            e = cudaOccupancyMaxActiveClusters(&n_pairs, gemm_bf16_sr_pair_kernel, &cfg);
-        }
+        if (e == cudaSuccess) e = pair_setup<4>(n_sms, &p4);
+        if (e == cudaSuccess) e = pair_setup<8>(n_sms, &p8);
         if (e != cudaSuccess) return cuda_fail(e);
         g_gemm_sms[dev] = n_sms;
-        g_gemm_pairs[dev] = n_pairs;
+        g_gemm_pairs[dev][0] = p4;
+        g_gemm_pairs[dev][1] = p8;
         g_gemm_ready[dev] = true;
     }
     *sms = g_gemm_sms[dev];
-    *pairs = g_gemm_pairs[dev];
+    pairs[0] = g_gemm_pairs[dev][0];
+    pairs[1] = g_gemm_pairs[dev][1];
     return ASR_OK;
+}
+
+template <int EPI>
+asr_status launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &P, uint64_t tiles,
+                       int pairs, cudaStream_t stream)
+{
+    const unsigned clusters = static_cast<unsigned>(tiles < static_cast<uint64_t>(pairs) ? tiles : pairs);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(PairShape<EPI>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const uint64_t limit = kWaitLimitNs;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel<EPI>, ma, mb, P, limit);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return check_launch();
 }
 
 // Row-major rows x k bf16 matrix, boxes of box_rows x 64 with 128-byte swizzle.
@@ -665,8 +715,8 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (m > (1u << 24) || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
         return ASR_ERR_INVALID_VALUE;
-    int sms = 0, pairs = 0;
-    asr_status st = device_setup(&sms, &pairs);
+    int sms = 0, pairs[2] = {0, 0};
+    asr_status st = device_setup(&sms, pairs);
     if (st != ASR_OK) return st;
     GemmParams P;
     P.c = c;
@@ -679,30 +729,16 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     P.keys = make_keys(seed);
     CUtensorMap ma, mb;
 #if ASR_GEMM_PAIR
-    if (pairs > 0) {
+    const bool wide = k <= static_cast<uint64_t>(kWideEpilogueMaxK);
+    if (pairs[wide ? 1 : 0] > 0) {
         // two-SM form: both operands in 128-row boxes (one half per CTA)
         st = make_map(&ma, a, m, k, 128);
         if (st == ASR_OK) st = make_map(&mb, b, n, k, 128);
         if (st != ASR_OK) return st;
         const uint64_t tiles = ((m + kPairBM - 1) / kPairBM) * ((n + kPairBN - 1) / kPairBN);
         if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
-        const unsigned clusters = static_cast<unsigned>(tiles < static_cast<uint64_t>(pairs) ? tiles : pairs);
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * clusters, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kPairSmem;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const uint64_t limit = kWaitLimitNs;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel, ma, mb, P, limit);
-        if (e != cudaSuccess) return cuda_fail(e);
-        return check_launch();
+        return wide ? launch_pair<8>(ma, mb, P, tiles, pairs[1], stream)
+                    : launch_pair<4>(ma, mb, P, tiles, pairs[0], stream);
     }
 #endif
     st = make_map(&ma, a, m, k, kBM);

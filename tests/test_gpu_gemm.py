@@ -6,6 +6,8 @@ checked against a binary64 product within the error bound of an f32 sum of K
 products; the bf16 output is then checked bit for bit against the oracle's
 rounding of that very accumulator (element (i, j) at global index i*N + j),
 which pins the epilogue exactly."""
+import os
+
 import numpy as np
 import pytest
 
@@ -48,7 +50,8 @@ def _check_accumulator(a, b, acc):
 
 
 @pytest.mark.parametrize("m,n,k", [(128, 128, 64), (256, 384, 512), (128, 256, 64 * 13), (1, 16, 8),
-                                   (200, 272, 520), (333, 1040, 72)])
+                                   (200, 272, 520), (333, 1040, 72),
+                                   (333, 1040, 1032)])
 @pytest.mark.parametrize("rounding", ["sr", "rne"])
 def test_gemm_matches_oracle_rounding_of_accumulator(asr, orc, m, n, k, rounding):
     import torch
@@ -142,3 +145,38 @@ def test_gemm_many_tiles_per_cta(asr, orc):
         want = orc.sr_fill(host(acc[int(i)]), int(i) * n, 2, 77)
         assert_same_bits(host(c[int(i)]), want, f"row {int(i)}", nan_equal=False)
     assert asr.asr_take_device_error() == 0
+
+
+def test_one_sm_kernel_variant(asr, orc, tmp_path):
+    """The one-SM 128 x 256 kernel, which the library falls back to where no
+    CTA pair fits, built alone (-DASR_GEMM_PAIR=0) into a separate library:
+    same bits as the oracle's rounding of its accumulator, ragged edges and
+    K tails included, and no device error."""
+    import ctypes
+    import subprocess
+    import torch
+    from stochastic_rounding_gb300 import build as B
+    so = str(tmp_path / "libasr_one_sm.so")
+    subprocess.run([B.nvcc(), *B.NVCC_FLAGS, "-DASR_GEMM_PAIR=0", "-I", os.path.join(B.ROOT, "include"),
+                    "-o", so, B.SRC], check=True)
+    L = ctypes.CDLL(so)
+    vp, u64, u32 = ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint32
+    L.asr_gemm_bf16_sr.argtypes = [vp, vp, vp, vp, u64, u64, u64, u32, u32, u64, vp]
+    L.asr_gemm_bf16_sr.restype = ctypes.c_int
+    L.asr_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+    L.asr_take_device_error.restype = ctypes.c_int
+    stream = torch.cuda.current_stream().cuda_stream
+    for (m, n, k) in [(128, 256, 64), (200, 272, 520), (1, 16, 8), (333, 1040, 72), (640, 768, 256)]:
+        a, b = _operands(m, n, k, seed=7 * m + n + k)
+        c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+        st = L.asr_gemm_bf16_sr(a.data_ptr(), b.data_ptr(), c.data_ptr(), acc.data_ptr(), m, n, k,
+                                0, 5, 2**33 + 1, stream)
+        assert st == 0, f"status {st}"
+        torch.cuda.synchronize()
+        _check_accumulator(a, b, acc)
+        want = orc.sr_fill(host(acc).reshape(-1), 0, 5, 2**33 + 1)
+        assert_same_bits(host(c).reshape(-1), want, f"one-SM gemm {m}x{n}x{k}", nan_equal=False)
+    bits = ctypes.c_uint32(0)
+    assert L.asr_take_device_error(ctypes.byref(bits), stream) == 0
+    assert bits.value == 0
