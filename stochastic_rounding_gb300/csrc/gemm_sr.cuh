@@ -121,8 +121,17 @@ struct GemmParams {
     uint32_t m, n, k;
     uint32_t step;
     uint32_t rounding;      // asr_rounding
+    uint32_t c_align32;     // c is 32-byte aligned: each lane's 16 outputs go out in one 256-bit store
     RoundKeys keys;
 };
+
+// One 256-bit store (sm_100 and later); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t w[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
 
 // Epilogue of one warp: accumulator row `row` of the output (this lane's
 // TMEM lane, columns from tq), columns n0 .. n0+ncols-1, rounded to bf16
@@ -152,9 +161,13 @@ __device__ __forceinline__ void store_rows(const GemmParams &P, uint32_t tq, uin
             for (int k = 0; k < 8; ++k)
                 w[k] = pack_bf16(round_rne(__uint_as_float(v[2 * k])), round_rne(__uint_as_float(v[2 * k + 1])));
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (P.c_align32) {
+            st_global_v8(P.c + e0, w);              // one full 32-byte sector per lane
+        } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(P.c + e0);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
         if (P.c_f32) {
             uint4 *df = reinterpret_cast<uint4 *>(P.c_f32 + e0);
 #pragma unroll
@@ -343,9 +356,10 @@ constexpr int kPairBN = 256;                // pair tile columns: B rows, 128 st
 // Same-run TFLOP/s (4 / 8 warps): 8192^2 x 1024: 972-986 / 1,096-1,141;
 // 8192^2 x 2048: 1,472-1,501 / 1,408-1,455; 8192^3: 1,716-1,764 / 1,730-1,759.
 constexpr int kWideEpilogueMaxK = 1024;
+constexpr int kWidestEpilogueMaxK = 512;
 template <int EPI>
 struct PairShape {
-    static_assert(EPI == 4 || EPI == 8, "epilogue warps: 4 or 8");
+    static_assert(EPI == 4 || EPI == 8 || EPI == 16, "epilogue warps: 4, 8 or 16");
     static constexpr int kThreads = 64 + 32 * EPI;     // producer warp, MMA warp, epilogue
     static constexpr int kSpan = 256 / (EPI / 4);      // columns per epilogue warp
 };
@@ -618,7 +632,7 @@ asr_status encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
 // odd number of SMs somewhere fewer than SMs/2 fit).
 bool g_gemm_ready[kMaxDevices];
 int g_gemm_sms[kMaxDevices];
-int g_gemm_pairs[kMaxDevices][2];
+int g_gemm_pairs[kMaxDevices][3];
 
 template <int EPI>
 cudaError_t pair_setup(int n_sms, int *n_pairs)
@@ -640,8 +654,8 @@ cudaError_t pair_setup(int n_sms, int *n_pairs)
     return cudaOccupancyMaxActiveClusters(n_pairs, gemm_bf16_sr_pair_kernel<EPI>, &cfg);
 }
 
-// pairs[0]: resident pairs of the 4-warp-epilogue kernel, pairs[1]: of the 8-warp one
-asr_status device_setup(int *sms, int pairs[2])
+// pairs[0], [1], [2]: resident pairs of the kernel with 4, 8, 16 epilogue warps
+asr_status device_setup(int *sms, int pairs[3])
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -650,19 +664,22 @@ asr_status device_setup(int *sms, int pairs[2])
     std::lock_guard<std::mutex> lk(g_encode_mu);
     if (!g_gemm_ready[dev]) {
         e = cudaFuncSetAttribute(gemm_bf16_sr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-        int n_sms = 0, p4 = 0, p8 = 0;
+        int n_sms = 0, p4 = 0, p8 = 0, p16 = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = pair_setup<4>(n_sms, &p4);
         if (e == cudaSuccess) e = pair_setup<8>(n_sms, &p8);
+        if (e == cudaSuccess) e = pair_setup<16>(n_sms, &p16);
         if (e != cudaSuccess) return cuda_fail(e);
         g_gemm_sms[dev] = n_sms;
         g_gemm_pairs[dev][0] = p4;
         g_gemm_pairs[dev][1] = p8;
+        g_gemm_pairs[dev][2] = p16;
         g_gemm_ready[dev] = true;
     }
     *sms = g_gemm_sms[dev];
     pairs[0] = g_gemm_pairs[dev][0];
     pairs[1] = g_gemm_pairs[dev][1];
+    pairs[2] = g_gemm_pairs[dev][2];
     return ASR_OK;
 }
 
@@ -715,7 +732,7 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (m > (1u << 24) || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
         return ASR_ERR_INVALID_VALUE;
-    int sms = 0, pairs[2] = {0, 0};
+    int sms = 0, pairs[3] = {0, 0, 0};
     asr_status st = device_setup(&sms, pairs);
     if (st != ASR_OK) return st;
     GemmParams P;
@@ -726,19 +743,24 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     P.k = static_cast<uint32_t>(k);
     P.step = step;
     P.rounding = rounding;
+    // rows are 32-byte multiples apart (n % 16 == 0), so every lane's
+    // 16-column piece is 32-byte aligned when c is
+    P.c_align32 = (reinterpret_cast<uintptr_t>(c) & 31u) == 0 ? 1u : 0u;
     P.keys = make_keys(seed);
     CUtensorMap ma, mb;
 #if ASR_GEMM_PAIR
-    const bool wide = k <= static_cast<uint64_t>(kWideEpilogueMaxK);
-    if (pairs[wide ? 1 : 0] > 0) {
+    const int shape = k <= static_cast<uint64_t>(kWidestEpilogueMaxK) ? 2
+                      : k <= static_cast<uint64_t>(kWideEpilogueMaxK) ? 1 : 0;
+    if (pairs[shape] > 0) {
         // two-SM form: both operands in 128-row boxes (one half per CTA)
         st = make_map(&ma, a, m, k, 128);
         if (st == ASR_OK) st = make_map(&mb, b, n, k, 128);
         if (st != ASR_OK) return st;
         const uint64_t tiles = ((m + kPairBM - 1) / kPairBM) * ((n + kPairBN - 1) / kPairBN);
         if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
-        return wide ? launch_pair<8>(ma, mb, P, tiles, pairs[1], stream)
-                    : launch_pair<4>(ma, mb, P, tiles, pairs[0], stream);
+        if (shape == 2) return launch_pair<16>(ma, mb, P, tiles, pairs[2], stream);
+        if (shape == 1) return launch_pair<8>(ma, mb, P, tiles, pairs[1], stream);
+        return launch_pair<4>(ma, mb, P, tiles, pairs[0], stream);
     }
 #endif
     st = make_map(&ma, a, m, k, kBM);

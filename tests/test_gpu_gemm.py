@@ -180,3 +180,22 @@ def test_one_sm_kernel_variant(asr, orc, tmp_path):
     bits = ctypes.c_uint32(0)
     assert L.asr_take_device_error(ctypes.byref(bits), stream) == 0
     assert bits.value == 0
+
+
+def test_output_only_16_byte_aligned(asr, orc):
+    """An output that starts 16 bytes past a 32-byte boundary takes the
+    128-bit store path (the 256-bit one needs 32-byte alignment): same bits,
+    and the words around the output stay untouched."""
+    import torch
+    m, n, k = 200, 272, 1032
+    a, b = _operands(m, n, k, seed=31)
+    buf = torch.full((m * n + 32,), 0x1234, dtype=torch.int16, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    c = buf[8:8 + m * n].view(torch.bfloat16).view(m, n)
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, rounding="sr", step=2, seed=99)
+    torch.cuda.synchronize()
+    want = orc.sr_fill(host(acc).reshape(-1), 0, 2, 99)
+    assert_same_bits(host(c).reshape(-1), want, "16-byte-aligned output", nan_equal=False)
+    h = host(buf)
+    assert (h[:8] == 0x1234).all() and (h[8 + m * n:] == 0x1234).all()
