@@ -34,7 +34,7 @@ METRIC = "AdamW-SR step Gparams/s and achieved HBM GB/s (% of GB300 peak), 1 GPU
 UNIT = "Gparams/s"
 BYTES_PER_PARAM = 22          # bf16 p r/w (2+2), bf16 g r (2), f32 m r/w (4+4), f32 v r/w (4+4)
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
-NORTH_STAR_PEAK_GBS = 8000.0
+NOMINAL_HBM_GBS = 8000.0
 # the device code of the AdamW-SR kernel: traffic figures are valid while
 # these files are unchanged
 KERNEL_SRC = [os.path.join(ROOT, "stochastic_rounding_gb300", "csrc", f)
@@ -475,7 +475,7 @@ def run_gpu(args):
                        "rounding": "stochastic (Philox4x32-10)", "bytes_per_param": BYTES_PER_PARAM,
                        "l2": "inputs larger than L2 (176.7 GB moved per step)",
                        "parallelism": f"shard{world}" if world > 1 else "single"},
-            "achieved_gbs": achieved, "frac_of_north_star_8tbs": achieved / NORTH_STAR_PEAK_GBS,
+            "achieved_gbs": achieved, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": tpp * n if tpp is not None else None,
