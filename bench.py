@@ -497,6 +497,25 @@ def run_gpu(args):
     return 0
 
 
+def gemm_cpu_baseline(a, b, m, n, k, budget_macs=6e9):
+    """The oracle's GEMM (binary64 sums of the exact products, one rounding
+    to binary32, the per-element stochastic rounding), single-threaded C,
+    timed on the first rows of the same operands: as many rows as fit in
+    about budget_macs multiply-adds."""
+    import numpy as np
+    import torch
+    import oracle
+    o = oracle.get()
+    rows = int(max(1, min(m, budget_macs // (n * k))))
+    a_h = a[:rows].cpu().view(torch.int16).numpy().view(np.uint16)
+    b_h = b.cpu().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    o.gemm_bf16(a_h, b_h, step=1, seed=0)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * n * k / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {m} rows x {n} columns x K={k}, C oracle single thread, {dt:.1f} s"}
+
+
 def run_gemm(args):
     """The tcgen05 GEMM with the stochastic-rounding epilogue (and with the
     round-to-nearest epilogue, and torch.matmul = cuBLAS, for context) on
@@ -536,12 +555,14 @@ def run_gemm(args):
     except Exception:
         peak, kind = 1900.0, "fallback"
     tf = flops / (t_sr / 1e3) / 1e12
+    cpu = gemm_cpu_baseline(a, b, m, n, k)
     line = {"metric": "bf16 GEMM with stochastic-rounding epilogue TFLOP/s", "value": tf, "unit": "TFLOP/s",
             "ms": t_sr, "config": {"workload": f"gemm {m}x{n}x{k} bf16, f32 accumulate, C = A.B^T"},
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                          "peak_kind": kind},
             "rne_epilogue_tflops": flops / (t_rn / 1e3) / 1e12,
             "cublas_torch_matmul_tflops": flops / (t_cublas / 1e3) / 1e12,
+            "cpu_baseline": cpu,
             "steps": args.steps, "warmup": args.warmup}
     print(json.dumps(line), flush=True)
     return 0

@@ -189,9 +189,10 @@ asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_
                                             const asr_adamw_hparams *hp, asr_stream_t stream);
 
 /* bf16 GEMM with a stochastic-rounding epilogue on the tensor cores ("Add
- * stochastic rounding and philox RNG helpers", Consumer: the bf16 GEMM's
- * f32 accumulator converts to bf16 by stochastic rounding, keyed per output
- * element from a seed, instead of round-to-nearest).
+ * stochastic rounding and philox RNG helpers", Consumer: the page's first
+ * user of the rounding is a bf16 matrix product whose binary32 sums may be
+ * written out by stochastic rounding, with random bits chosen per output
+ * element from a seed, as an alternative to the default nearest rounding).
  * C = A . B^T with A: m x k, B: n x k, C: m x n, all row-major bf16 patterns
  * (device, caller-owned); f32 accumulation.  Output element (i, j) is
  * rounded from its f32 accumulator acc(i, j) exactly as

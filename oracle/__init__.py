@@ -53,6 +53,10 @@ class Oracle:
         L.oracle_sr_fill.argtypes = [F32P, U32P, U16P, ctypes.c_uint64, ctypes.c_uint64,
                                      ctypes.c_uint32, ctypes.c_uint64]
         L.oracle_sr_fill.restype = None
+        L.oracle_gemm_bf16.argtypes = [U16P, U16P, F32P, U16P, ctypes.c_uint64, ctypes.c_uint64,
+                                       ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
+                                       ctypes.c_uint32, ctypes.c_uint64]
+        L.oracle_gemm_bf16.restype = None
         L.oracle_adamw_scalars.argtypes = [ctypes.c_double] * 5 + [ctypes.c_uint32, F32P]
         L.oracle_adamw_scalars.restype = None
         L.oracle_adamw_step.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
@@ -114,6 +118,23 @@ class Oracle:
         self.lib.oracle_sr_fill(_ptr(x, F32P), _ptr(rb, U32P) if rb is not None else None,
                                 _ptr(out, U16P), x.size, int(base_index), int(step), int(seed))
         return out
+
+    # -- GEMM -----------------------------------------------------------------
+    def gemm_bf16(self, a, b, *, row0=0, rounding=ROUND_SR, step=0, seed=0):
+        """Rows row0 .. row0+m-1 of C = A.B^T rounded to bf16, and their
+        binary32 accumulators: ``a`` (m x k) and ``b`` (n x k) uint16 arrays of
+        bf16 patterns.  Returns (out uint16 (m, n), acc float32 (m, n))."""
+        a = np.ascontiguousarray(a, dtype=np.uint16)
+        b = np.ascontiguousarray(b, dtype=np.uint16)
+        if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+            raise ValueError("a is m x k and b is n x k")
+        m, k = a.shape
+        n = b.shape[0]
+        out = np.zeros((m, n), dtype=np.uint16)
+        acc = np.zeros((m, n), dtype=np.float32)
+        self.lib.oracle_gemm_bf16(_ptr(a, U16P), _ptr(b, U16P), _ptr(acc, F32P), _ptr(out, U16P),
+                                  m, n, k, int(row0), int(rounding), int(step), int(seed))
+        return out, acc
 
     # -- AdamW ----------------------------------------------------------------
     def adamw_scalars(self, lr, beta1, beta2, eps, weight_decay, step):

@@ -26,6 +26,11 @@
  *          Philox keyed by (seed, step) and indexed by each element's global
  *          parameter position; section Correctness: shards with base_index equal
  *          the whole update.  Loshchilov and Hutter (2019) for AdamW itself.
+ *   [GEMM] "Add stochastic rounding and philox RNG helpers", section Consumer:
+ *          the rounding's first user, a bf16 matrix product that may write
+ *          its binary32 sums out by stochastic rounding, random bits chosen
+ *          per output element from a seed, as an option next to nearest
+ *          rounding.
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - counter layout: key = (seed lo, seed hi); counter = ((i>>2) lo, (i>>2) hi,
@@ -161,6 +166,34 @@ void oracle_sr_fill(const float *x, const uint32_t *rbits, uint16_t *out, uint64
     for (uint64_t j = 0; j < n; ++j) {
         uint32_t r = rbits ? rbits[j] : oracle_element_word(base_index + j, step, seed);
         out[j] = oracle_sr_bf16(x[j], r);
+    }
+}
+
+/* ----------------------------------------------------------------- GEMM ---- */
+
+/* [GEMM] C = A . B^T, A (m x k) and B (n x k) row-major bf16 patterns, rows
+ * row0 .. row0+m-1 of a product with n columns.  The page fixes no summation
+ * order, so the accumulator here is the plain definition: the binary64 sum,
+ * in k order, of the bf16 x bf16 products (each exact in binary64), rounded
+ * once to binary32.  Element (row0 + i, j) has global index (row0 + i)*n + j
+ * and is rounded like every other element of this file: stochastically with
+ * its Philox word (rounding 0) or to nearest-even (rounding 1).  acc, if
+ * non-NULL, receives the binary32 accumulator. */
+void oracle_gemm_bf16(const uint16_t *a, const uint16_t *b, float *acc, uint16_t *out, uint64_t m,
+                      uint64_t n, uint64_t k, uint64_t row0, int rounding, uint32_t step, uint64_t seed)
+{
+    for (uint64_t i = 0; i < m; ++i) {
+        for (uint64_t j = 0; j < n; ++j) {
+            double s = 0.0;
+            for (uint64_t t = 0; t < k; ++t)
+                s += (double)bf16_to_f32(a[i * k + t]) * (double)bf16_to_f32(b[j * k + t]);
+            const float x = (float)s;
+            if (acc)
+                acc[i * n + j] = x;
+            out[i * n + j] = rounding == 1
+                ? oracle_rne_bf16(x)
+                : oracle_sr_bf16(x, oracle_element_word((row0 + i) * n + j, step, seed));
+        }
     }
 }
 

@@ -4,9 +4,9 @@
 // device error word with the optimizer kernels.
 //
 // "Add stochastic rounding and philox RNG helpers" (FlyDSL PR 907), section
-// Consumer: a bf16 GEMM gains a rounding option; with stochastic rounding the
-// f32 accumulator converts to bf16 through stochastic rounding, keyed per
-// output element from a seed, instead of round-to-nearest.  Here output
+// Consumer: the first user of the rounding is a bf16 matrix product that may
+// write its binary32 sums out by stochastic rounding, random bits chosen per
+// output element from a seed, as an option next to nearest rounding.  Here output
 // element (i, j) of the M x N result has global index i*N + j and draws its
 // random bits exactly as every other element of this library does: word
 // (e & 3) of Philox4x32-10 at counter ((e>>2) lo, (e>>2) hi, step, 0) under

@@ -9,7 +9,7 @@ What pins what:
   * Philox4x32-10: Triton's library Philox (``tl.philox``, run in its CPU
     interpreter) on random counters and 64-bit keys; statistics of the stream
     ("Add stochastic rounding and philox RNG helpers", Tests: uniform and
-    collision-free).
+    free of repeats).
   * element -> (counter, word) mapping: the same independent Philox on the
     counter ((i>>2) lo, (i>>2) hi, step, 0) and key (seed lo, seed hi).
   * stochastic rounding: the exhaustive closed forms of the same page's Tests
@@ -21,6 +21,12 @@ What pins what:
     special cases with closed forms (no gradient; first step; eps-dominated).
   * the sub-ULP demonstration ("adamw-sr", introduction; tests/golden).
   * shard invariance ("adamw-sr", Method and Correctness).
+  * the bf16 GEMM with a stochastic-rounding epilogue ("Add stochastic
+    rounding and philox RNG helpers", Consumer): exact rational sums of tiny
+    non-square products (Python fractions), rounded once to binary32, then
+    each element rounded with its own Philox word; closed forms where the
+    product is exactly a bf16 value (one-hot rows pick elements of B; small
+    integer sums), which every seed and both roundings must reproduce.
 """
 import json
 import os
@@ -547,3 +553,71 @@ def pin_no_contraction(o):
     a = float(np.float32(1 + 2**-12))
     c = float(np.float32(-(1 + 2**-11)))
     assert o.mul_add(a, a, c) == 0.0
+
+
+# --------------------------------------------------------------------------
+# bf16 GEMM with a stochastic-rounding epilogue ("Add stochastic rounding and
+# philox RNG helpers", Consumer)
+# --------------------------------------------------------------------------
+
+def _bf16_grid(rng, shape, emin=-6, emax=6):
+    """bf16 patterns of values m * 2^e, |m| < 256 an integer, e in [emin, emax]:
+    sums of a few such products are exact in binary64."""
+    mant = rng.integers(-255, 256, size=shape).astype(np.float64)
+    expo = rng.integers(emin, emax + 1, size=shape).astype(np.float64)
+    return W.to_bf16_bits((mant * 2.0 ** (expo - 7)).astype(np.float32))
+
+
+def pin_gemm_exact_small(o, seed=5):
+    """C = A.B^T on 3 x 7 by 5 x 7 operands (non-square: a transposed operand
+    or a swapped index cannot pass): the accumulator equals the exact rational
+    sum rounded once to binary32; element (row0+i, j) is rounded with word
+    (row0+i)*n + j of the Philox stream (or to nearest-even); computing the
+    rows from row0 in two slices gives the same bits as the whole."""
+    from fractions import Fraction
+    rng = np.random.default_rng(seed)
+    m, n, k = 3, 5, 7
+    a = _bf16_grid(rng, (m, k))
+    b = _bf16_grid(rng, (n, k))
+    av, bv = bf16_value(a), bf16_value(b)
+    exact = np.zeros((m, n), dtype=np.float32)
+    for i in range(m):
+        for j in range(n):
+            s = sum((Fraction(float(av[i, t])) * Fraction(float(bv[j, t])) for t in range(k)), Fraction(0))
+            exact[i, j] = np.float32(float(s))          # float(s) is exact here; one rounding to binary32
+    row0, step, seed_ = 1000, 9, 2**37 + 5
+    out, acc = o.gemm_bf16(a, b, row0=row0, step=step, seed=seed_)
+    assert np.array_equal(bits_from_f32(acc), bits_from_f32(exact)), "accumulator is not the exact sum"
+    for i in range(m):
+        for j in range(n):
+            r = o.element_word((row0 + i) * n + j, step, seed_)
+            assert int(out[i, j]) == o.sr_bf16(exact[i, j], r), f"SR element ({i}, {j})"
+    out_rn, _ = o.gemm_bf16(a, b, row0=row0, rounding=1)
+    assert np.array_equal(out_rn, o.rne_fill(exact)), "RNE epilogue"
+    top, _ = o.gemm_bf16(a[:1], b, row0=row0, step=step, seed=seed_)
+    rest, _ = o.gemm_bf16(a[1:], b, row0=row0 + 1, step=step, seed=seed_)
+    assert np.array_equal(np.vstack([top, rest]), out), "row slices differ from the whole"
+
+
+def pin_gemm_closed_forms(o, seed=6):
+    """Products that are exactly bf16 values come out unchanged for every
+    seed and both roundings: (a) one-hot rows of A pick C[i, j] = B[j, sel_i];
+    (b) entries in {-2..2} with k = 24 give integer sums |s| <= 96."""
+    rng = np.random.default_rng(seed)
+    m, n, k = 6, 10, 12
+    sel = rng.integers(0, k, size=m)
+    a = np.zeros((m, k), dtype=np.uint16)
+    a[np.arange(m), sel] = 0x3F80                                   # 1.0
+    b = W.to_bf16_bits(rng.normal(0.0, 3.0, size=(n, k)).astype(np.float32))
+    want = b[:, sel].T.copy()
+    for s_ in (0, 1, 2**63 + 11):
+        out, _ = o.gemm_bf16(a, b, row0=17, step=3, seed=s_)
+        assert np.array_equal(out, want), f"one-hot rows, seed {s_}"
+    out, _ = o.gemm_bf16(a, b, rounding=1)
+    assert np.array_equal(out, want), "one-hot rows, RNE"
+    ai = rng.integers(-2, 3, size=(7, 24)).astype(np.float32)
+    bi = rng.integers(-2, 3, size=(9, 24)).astype(np.float32)
+    want = W.to_bf16_bits((ai @ bi.T).astype(np.float32))
+    for s_ in (4, 5):
+        out, _ = o.gemm_bf16(W.to_bf16_bits(ai), W.to_bf16_bits(bi), step=1, seed=s_)
+        assert np.array_equal(out, want), f"integer sums, seed {s_}"

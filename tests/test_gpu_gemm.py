@@ -199,3 +199,42 @@ def test_output_only_16_byte_aligned(asr, orc):
     assert_same_bits(host(c).reshape(-1), want, "16-byte-aligned output", nan_equal=False)
     h = host(buf)
     assert (h[:8] == 0x1234).all() and (h[8 + m * n:] == 0x1234).all()
+
+
+@pytest.mark.parametrize("m,n,k", [(200, 272, 520), (333, 1040, 1032), (1, 16, 8), (512, 1024, 64)])
+@pytest.mark.parametrize("rounding", ["sr", "rne"])
+def test_gemm_equals_oracle_gemm_on_integer_operands(asr, orc, m, n, k, rounding):
+    """Entries in {-8..8}: every partial sum is an integer below 2^24, exact in
+    binary32 whatever the summation order, so the kernel's accumulator must
+    equal the oracle GEMM's bit for bit, and so must the whole bf16 output
+    (sums above 256 are not bf16 values: the rounding draws real bits)."""
+    import torch
+    g = torch.Generator(device="cuda")
+    g.manual_seed(m * 7 + k)
+    a = torch.randint(-8, 9, (m, k), device="cuda", generator=g).to(torch.bfloat16)
+    b = torch.randint(-8, 9, (n, k), device="cuda", generator=g).to(torch.bfloat16)
+    c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, rounding=rounding, step=4, seed=1234)
+    torch.cuda.synchronize()
+    want, want_acc = orc.gemm_bf16(host(a), host(b), rounding=0 if rounding == "sr" else 1, step=4, seed=1234)
+    assert np.array_equal(host(acc).view(np.uint32), want_acc.view(np.uint32)), "accumulators differ"
+    assert_same_bits(host(c), want, f"gemm {m}x{n}x{k} {rounding} vs oracle GEMM", nan_equal=False)
+
+
+def test_gemm_against_oracle_gemm(asr, orc):
+    """Normal operands: the accumulators differ only by summation order
+    (within the bound), and wherever they are equal the bf16 outputs are
+    identical (same keying)."""
+    import torch
+    m, n, k = 200, 272, 520
+    a, b = _operands(m, n, k, seed=41)
+    c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, rounding="sr", step=4, seed=1234)
+    torch.cuda.synchronize()
+    want, want_acc = orc.gemm_bf16(host(a), host(b), step=4, seed=1234)
+    _check_accumulator(a, b, acc)
+    same = host(acc).view(np.uint32) == want_acc.view(np.uint32)
+    assert same.sum() >= 100, f"only {same.sum()} accumulators agree bitwise"
+    assert np.array_equal(host(c)[same], want[same]), "same accumulator, different rounding"

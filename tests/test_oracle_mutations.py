@@ -50,6 +50,15 @@ MUTATIONS = [
      ["adamw", "adamw_special"]),
     ("gradient not squared", "float gg = g * g;", "float gg = g;", ["adamw", "adamw_special"]),
     ("old first moment written back", "exp_avg[j] = m1;", "exp_avg[j] = m;", ["adamw", "adamw_special"]),
+    ("gemm reads B transposed", "(double)bf16_to_f32(b[j * k + t])", "(double)bf16_to_f32(b[t * n + j])",
+     ["gemm"]),
+    ("gemm drops the last product", "for (uint64_t t = 0; t < k; ++t)", "for (uint64_t t = 0; t + 1 < k; ++t)",
+     ["gemm"]),
+    ("gemm accumulates in binary32", "            double s = 0.0;", "            float s = 0.0f;", ["gemm"]),
+    ("gemm keys by the slice row", "oracle_element_word((row0 + i) * n + j, step, seed)",
+     "oracle_element_word(i * n + j, step, seed)", ["gemm"]),
+    ("gemm keys by column-major index", "oracle_element_word((row0 + i) * n + j, step, seed)",
+     "oracle_element_word(j * (row0 + m) + row0 + i, step, seed)", ["gemm"]),
     ("base_index ignored", "oracle_element_word(base_index + j, step, seed));\n            ((uint16_t",
      "oracle_element_word(j, step, seed));\n            ((uint16_t", ["dtype", "shards"]),
 ]
@@ -68,6 +77,7 @@ def _run_pins(o, which, philox_ref):
                           lambda: pins.pin_adamw_one_step_tight(o)],
         "dtype": [lambda: pins.pin_adamw_dtype_paths(o)],
         "shards": [lambda: pins.pin_shard_invariance(o)],
+        "gemm": [lambda: pins.pin_gemm_exact_small(o), lambda: pins.pin_gemm_closed_forms(o)],
     }
     for g in which:
         for f in groups[g]:

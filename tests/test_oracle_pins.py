@@ -76,3 +76,11 @@ def test_shard_invariance(orc):
 
 def test_no_fp_contraction(orc):
     pins.pin_no_contraction(orc)
+
+
+def test_gemm_exact_small(orc):
+    pins.pin_gemm_exact_small(orc)
+
+
+def test_gemm_closed_forms(orc):
+    pins.pin_gemm_closed_forms(orc)
