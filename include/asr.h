@@ -6,8 +6,9 @@
  *   "Add stochastic rounding and philox RNG helpers" (FlyDSL PR 907),
  *       section Primitives -- stochastic rounding f32 -> bf16 and the Philox
  *       4x32 counter-based generator that feeds it;
- *   "adamw-sr", introduction and sections Method / Correctness -- the fused
- *       decoupled-weight-decay Adam step with bf16 stochastic write-back, its
+ *   "adamw-sr", introduction and sections Method / Correctness -- one fused
+ *       AdamW (Adam with decoupled weight decay) pass with bf16 parameters
+ *       written back by stochastic rounding, its
  *       randomness keyed by (seed, step) and indexed by each element's global
  *       parameter position, identical whole or in shards with a base_index.
  *

@@ -1,6 +1,7 @@
 """The AdamWSR optimizer class ("adamw-sr", Usage) and the bf16-only
-training claim ("adamw-sr", Correctness: a bf16-only layer with no fp32
-master converges with SR and out-trains round-to-nearest)."""
+training claim ("adamw-sr", Correctness: a layer kept only in bf16, with no
+fp32 master copy, still learns under SR and ends with a lower loss than under
+nearest rounding)."""
 import io
 
 import numpy as np
