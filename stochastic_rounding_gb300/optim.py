@@ -1,10 +1,11 @@
 """``AdamWSR``: a torch optimizer over the fused AdamW-SR kernels.
 
-"adamw-sr", section Usage: a drop-in for ``torch.optim.AdamW`` whose states
-are float32, whose parameters may be float32 or bfloat16 (bf16 ones written
-back by stochastic rounding, no fp32 master copy) and whose gradients may be
-float32 or bfloat16.  Section Method: the rounding bits are keyed by
-(seed, step) and indexed by each element's global parameter position.
+"adamw-sr", section Usage: it takes the place of ``torch.optim.AdamW`` with
+the same arguments plus a seed.  Moment buffers are kept in float32;
+parameters are float32 or bfloat16, the bfloat16 ones updated in place by
+stochastic rounding with no float32 copy kept; gradients are float32 or
+bfloat16.  Section Method: the rounding bits are keyed by (seed, step) and
+indexed by each element's global parameter position.
 
 Global positions: the parameters, in the order the optimizer was given them
 (all groups, in group order), are laid end to end; a parameter's base index
