@@ -568,6 +568,70 @@ def run_gemm(args):
     return 0
 
 
+def run_elementwise(args):
+    """The stand-alone rounding op (--sr N: float32 -> bf16 with Philox bits,
+    6 B per element) or the Philox op (--philox N: N counters, 16 B written
+    each) over N elements resident in HBM (larger than L2), by CUDA events
+    over the timed launches, against the measured copy bandwidth; the oracle
+    on a 2^22-element sample beside it."""
+    import numpy as np
+    import torch
+    from __graft_entry__ import build
+    build()
+    import stochastic_rounding_gb300 as asr
+    import oracle
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.sr:
+        n, unit_bytes, what = args.sr, 6, "stand-alone stochastic rounding float32 -> bf16"
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        x = torch.randn(n, device=dev, generator=g)
+        out = torch.empty(n, device=dev, dtype=torch.bfloat16)
+        fn = lambda: asr.asr_stochastic_round_bf16(x, out, base_index=0, step=1, seed=0)
+    else:
+        n, unit_bytes, what = args.philox, 16, "Philox4x32-10 counters, four words each"
+        out = torch.empty(4 * n, device=dev, dtype=torch.int32)
+        fn = lambda: asr.asr_philox4x32(out, n, 0, 1, 0, 0)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    err = asr.asr_take_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+    peak, kind = measured_peak()
+    gbs = unit_bytes * n / (ms / 1e3) / 1e9
+    o = oracle.get()
+    sample = 1 << 22
+    t0 = time.perf_counter()
+    if args.sr:
+        o.sr_fill(x[:sample].cpu().numpy(), 0, 1, 0)
+    else:
+        o.philox_fill(sample, 0, 1, 0, 0)
+    dt = time.perf_counter() - t0
+    unit = "Gelem/s" if args.sr else "Gctr/s"
+    line = {"metric": f"{what} {unit}", "value": n / (ms / 1e3) / 1e9, "unit": unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "f32->bf16" if args.sr else "u32", "data": "synthetic",
+            "config": {"workload": f"{what}, {n:,} {'elements' if args.sr else 'counters'}",
+                       "l2": "inputs and outputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_kind": kind, "bytes_per_unit": unit_bytes},
+            "cpu_baseline": {"value": sample / dt / 1e9, "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": f"{sample:,} {'elements' if args.sr else 'counters'}, C oracle single thread"},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -579,9 +643,15 @@ def main():
                          "(a small case for profiling); 0 = the full set")
     ap.add_argument("--gemm", type=int, nargs=3, metavar=("M", "N", "K"), default=None,
                     help="time the tensor-core GEMM with the stochastic-rounding epilogue instead")
+    ap.add_argument("--sr", type=int, default=0, metavar="N",
+                    help="time the stand-alone stochastic-rounding op on N float32 elements instead")
+    ap.add_argument("--philox", type=int, default=0, metavar="N",
+                    help="time the Philox op on N counters instead")
     args = ap.parse_args()
     if args.gemm:
         return run_gemm(args)
+    if args.sr or args.philox:
+        return run_elementwise(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
