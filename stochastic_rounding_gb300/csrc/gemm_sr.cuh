@@ -122,6 +122,9 @@ struct GemmParams {
     uint32_t step;
     uint32_t rounding;      // asr_rounding
     uint32_t c_align32;     // c is 32-byte aligned: each lane's 16 outputs go out in one 256-bit store
+    // two-SM kernel: the first `wide` work items are 256 x 256 tiles, the
+    // next `narrow` are the halves (256 x 128) of the last narrow/2 tiles
+    uint32_t wide, narrow;
     RoundKeys keys;
 };
 
@@ -370,8 +373,34 @@ constexpr uint32_t kHalfB = 128 * kBK * 2;          // 16 KB per CTA
 constexpr uint32_t kPairStageBytes = kHalfA + kHalfB;
 // barriers: full/empty per stage, full/empty per accumulator, the MMA drain
 constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + (2 * kPairStages + 2 * kAccBufs + 1) * 8 + 16;
-constexpr uint32_t kPairInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kPairBN >> 3) << 17) |
-                                    (uint32_t(kPairBM >> 4) << 24);
+constexpr uint32_t pair_instr_desc(uint32_t n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (uint32_t(kPairBM >> 4) << 24);
+}
+constexpr uint32_t kPairInstrDesc = pair_instr_desc(kPairBN);           // M=256, N=256
+constexpr uint32_t kPairInstrDescNarrow = pair_instr_desc(kPairBN / 2); // M=256, N=128
+
+// Work item t of the pair schedule: its tile's first row and column and its
+// width.  Items below P.wide are whole tiles in the grouped order; item
+// P.wide + u is half (u & 1) of whole tile P.wide + u/2.  Splitting the tiles
+// of a last, partly filled round in two (when their halves still fit in one
+// round) halves that round's length.
+__device__ __forceinline__ void pair_item(const GemmParams &P, uint32_t t, uint32_t tiles_m, uint32_t tiles_n,
+                                          uint32_t &m0, uint32_t &n0, uint32_t &width)
+{
+    uint32_t mt, nt;
+    if (t < P.wide) {
+        tile_coords(t, tiles_m, tiles_n, mt, nt, kPairGroupM);
+        n0 = nt * kPairBN;
+        width = kPairBN;
+    } else {
+        const uint32_t u = t - P.wide;
+        tile_coords(P.wide + u / 2, tiles_m, tiles_n, mt, nt, kPairGroupM);
+        n0 = nt * kPairBN + (u & 1u) * (kPairBN / 2);
+        width = kPairBN / 2;
+    }
+    m0 = mt * kPairBM;
+}
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -435,13 +464,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kPairInstrDesc), "r"(accumulate)
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -460,7 +490,8 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar)
 template <int EPI>
 __global__ void __launch_bounds__(PairShape<EPI>::kThreads, 1)
 gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                         const __grid_constant__ GemmParams P, uint64_t limit_ns)
+                         const __grid_constant__ CUtensorMap map_b_half, const __grid_constant__ GemmParams P,
+                         uint64_t limit_ns)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -479,7 +510,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
     const bool leader = rank == 0;
     const uint32_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
     const uint32_t tiles_m = (P.m + kPairBM - 1) / kPairBM, tiles_n = (P.n + kPairBN - 1) / kPairBN;
-    const uint32_t tiles = tiles_m * tiles_n;
+    const uint32_t items = P.wide + P.narrow;
     const int kblocks = static_cast<int>((P.k + kBK - 1) / kBK);
 
     if (threadIdx.x == 0) {
@@ -510,12 +541,14 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         // ------------------------------------------------------- producer
         uint32_t g = 0;
         bool ok = true;
-        for (uint32_t t = cluster; ok && t < tiles; t += clusters) {
-            uint32_t mt, nt;
-            tile_coords(t, tiles_m, tiles_n, mt, nt, kPairGroupM);
-            uint32_t ra = mt * kPairBM + rank * 128, rb = nt * kPairBN + rank * 128;
+        for (uint32_t t = cluster; ok && t < items; t += clusters) {
+            uint32_t m0, n0, width;
+            pair_item(P, t, tiles_m, tiles_n, m0, n0, width);
+            const bool half = width != kPairBN;             // each CTA stages 64 rows of B, not 128
+            uint32_t ra = m0 + rank * 128, rb = n0 + rank * (width / 2);
             if (ra >= P.m) ra = 0;
             if (rb >= P.n) rb = 0;
+            const uint32_t bytes = 2 * (kHalfA + (half ? kHalfB / 2 : kHalfB));
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int s = static_cast<int>(g % kPairStages);
                 const uint32_t use = g / kPairStages;
@@ -523,11 +556,11 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
                     ok = false;
                     break;
                 }
-                if (leader) mbar_arrive_expect_tx(full(s), 2 * kPairStageBytes);
+                if (leader) mbar_arrive_expect_tx(full(s), bytes);
                 const uint32_t bar = peer_addr(full(s), 0);
                 const uint32_t dst = base + s * kPairStageBytes;
                 tma_load_2d_pair(dst, &map_a, kb * kBK, static_cast<int32_t>(ra), bar);
-                tma_load_2d_pair(dst + kHalfA, &map_b, kb * kBK, static_cast<int32_t>(rb), bar);
+                tma_load_2d_pair(dst + kHalfA, half ? &map_b_half : &map_b, kb * kBK, static_cast<int32_t>(rb), bar);
             }
         }
         // the MMAs that read this CTA's stages have completed, and their
@@ -540,12 +573,13 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         // ------------------------------------------------------ MMA issuer
         uint32_t g = 0, i = 0;
         bool ok = true;
-        for (uint32_t t = cluster; ok && t < tiles; t += clusters, ++i) {
+        for (uint32_t t = cluster; ok && t < items; t += clusters, ++i) {
             const int b = static_cast<int>(i % kAccBufs);
             const uint32_t ub = i / kAccBufs;
             if (ub > 0 && !mbar_wait_cluster(acc_empty(b), (ub - 1) & 1u, limit_ns)) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t d = tmem + static_cast<uint32_t>(b * kPairBN);
+            const uint32_t idesc = t < P.wide ? kPairInstrDesc : kPairInstrDescNarrow;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int s = static_cast<int>(g % kPairStages);
                 const uint32_t use = g / kPairStages;
@@ -557,7 +591,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
                 const uint32_t sa = base + s * kPairStageBytes, sb = sa + kHalfA;
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_bf16_pair(d, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), (kb | kk) != 0);
+                    mma_bf16_pair(d, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), idesc, (kb | kk) != 0);
                 mma_commit_pair(empty(s));
             }
             mma_commit_pair(acc_full(b));
@@ -575,18 +609,18 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         constexpr int kSpan = PairShape<EPI>::kSpan;
         const int c_lo = ((warp - 2) / 4) * kSpan;
         uint32_t i = 0;
-        for (uint32_t t = cluster; t < tiles; t += clusters, ++i) {
+        for (uint32_t t = cluster; t < items; t += clusters, ++i) {
             const int b = static_cast<int>(i % kAccBufs);
             const uint32_t ub = i / kAccBufs;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(b), ub & 1u, limit_ns))) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            uint32_t mt, nt;
-            tile_coords(t, tiles_m, tiles_n, mt, nt, kPairGroupM);
-            const uint32_t row = mt * kPairBM + rank * 128 + quarter * 32 + lane;
-            const uint32_t n0 = nt * kPairBN;
+            uint32_t m0, n0, width;
+            pair_item(P, t, tiles_m, tiles_n, m0, n0, width);
+            const uint32_t row = m0 + rank * 128 + quarter * 32 + lane;
             const uint32_t tq =
                 tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(b * kPairBN);
-            const int ncols = static_cast<int>(P.n - n0) < kPairBN ? static_cast<int>(P.n - n0) : kPairBN;
+            // the second half of a tile can lie wholly past N: nothing to store
+            const int ncols = n0 >= P.n ? 0 : P.n - n0 < width ? static_cast<int>(P.n - n0) : static_cast<int>(width);
             const int c_hi = ncols < c_lo + kSpan ? ncols : c_lo + kSpan;
             if (c_hi > c_lo) store_rows(P, tq + c_lo, row, n0 + c_lo, c_hi - c_lo);
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -683,11 +717,26 @@ asr_status device_setup(int *sms, int pairs[3])
     return ASR_OK;
 }
 
-template <int EPI>
-asr_status launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &P, uint64_t tiles,
-                       int pairs, cudaStream_t stream)
+// The pair schedule for `tiles` whole tiles on up to `pairs` resident pairs:
+// whole tiles round by round; if the last round is at most half full, its
+// tiles go as halves (twice the items, each half as long), so the round
+// takes half the time.  Returns the number of clusters to launch.
+unsigned pair_schedule(uint64_t tiles, uint64_t pairs, GemmParams &P)
 {
-    const unsigned clusters = static_cast<unsigned>(tiles < static_cast<uint64_t>(pairs) ? tiles : pairs);
+    uint64_t rest = tiles % pairs;                   // tiles of the last, partly filled round
+    if (tiles < pairs) rest = tiles;
+    const bool split = rest > 0 && 2 * rest <= pairs;
+    P.wide = static_cast<uint32_t>(tiles - (split ? rest : 0));
+    P.narrow = static_cast<uint32_t>(split ? 2 * rest : 0);
+    const uint64_t items = P.wide + static_cast<uint64_t>(P.narrow);
+    return static_cast<unsigned>(items < pairs ? items : pairs);
+}
+
+template <int EPI>
+asr_status launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mb_half, GemmParams &P,
+                       uint64_t tiles, int pairs, cudaStream_t stream)
+{
+    const unsigned clusters = pair_schedule(tiles, static_cast<uint64_t>(pairs), P);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -701,7 +750,7 @@ asr_status launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const GemmP
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const uint64_t limit = kWaitLimitNs;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel<EPI>, ma, mb, P, limit);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel<EPI>, ma, mb, mb_half, P, limit);
     if (e != cudaSuccess) return cuda_fail(e);
     return check_launch();
 }
@@ -746,6 +795,8 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     // rows are 32-byte multiples apart (n % 16 == 0), so every lane's
     // 16-column piece is 32-byte aligned when c is
     P.c_align32 = (reinterpret_cast<uintptr_t>(c) & 31u) == 0 ? 1u : 0u;
+    P.wide = 0;
+    P.narrow = 0;
     P.keys = make_keys(seed);
     CUtensorMap ma, mb;
 #if ASR_GEMM_PAIR
@@ -753,14 +804,16 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
                       : k <= static_cast<uint64_t>(kWideEpilogueMaxK) ? 1 : 0;
     if (pairs[shape] > 0) {
         // two-SM form: both operands in 128-row boxes (one half per CTA)
+        CUtensorMap mb_half;
         st = make_map(&ma, a, m, k, 128);
         if (st == ASR_OK) st = make_map(&mb, b, n, k, 128);
+        if (st == ASR_OK) st = make_map(&mb_half, b, n, k, 64);     // B halves of split tiles
         if (st != ASR_OK) return st;
         const uint64_t tiles = ((m + kPairBM - 1) / kPairBM) * ((n + kPairBN - 1) / kPairBN);
         if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
-        if (shape == 2) return launch_pair<16>(ma, mb, P, tiles, pairs[2], stream);
-        if (shape == 1) return launch_pair<8>(ma, mb, P, tiles, pairs[1], stream);
-        return launch_pair<4>(ma, mb, P, tiles, pairs[0], stream);
+        if (shape == 2) return launch_pair<16>(ma, mb, mb_half, P, tiles, pairs[2], stream);
+        if (shape == 1) return launch_pair<8>(ma, mb, mb_half, P, tiles, pairs[1], stream);
+        return launch_pair<4>(ma, mb, mb_half, P, tiles, pairs[0], stream);
     }
 #endif
     st = make_map(&ma, a, m, k, kBM);

@@ -51,7 +51,7 @@ def _check_accumulator(a, b, acc):
 
 @pytest.mark.parametrize("m,n,k", [(128, 128, 64), (256, 384, 512), (128, 256, 64 * 13), (1, 16, 8),
                                    (200, 272, 520), (333, 1040, 72),
-                                   (333, 1040, 1032)])
+                                   (333, 1040, 1032), (1800, 1296, 136)])
 @pytest.mark.parametrize("rounding", ["sr", "rne"])
 def test_gemm_matches_oracle_rounding_of_accumulator(asr, orc, m, n, k, rounding):
     import torch
@@ -201,7 +201,8 @@ def test_output_only_16_byte_aligned(asr, orc):
     assert (h[:8] == 0x1234).all() and (h[8 + m * n:] == 0x1234).all()
 
 
-@pytest.mark.parametrize("m,n,k", [(200, 272, 520), (333, 1040, 1032), (1, 16, 8), (512, 1024, 64)])
+@pytest.mark.parametrize("m,n,k", [(200, 272, 520), (333, 1040, 1032), (1, 16, 8), (512, 1024, 64),
+                                   (1800, 1296, 136), (4096, 4096, 64)])
 @pytest.mark.parametrize("rounding", ["sr", "rne"])
 def test_gemm_equals_oracle_gemm_on_integer_operands(asr, orc, m, n, k, rounding):
     """Entries in {-8..8}: every partial sum is an integer below 2^24, exact in
