@@ -8,6 +8,7 @@ missing or a call fails, an exception is raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional, Sequence
@@ -109,7 +110,7 @@ def asr_take_device_error(stream=None, device=None) -> int:
     torch = _torch()
     dev = torch.device(device if device is not None else "cuda")
     bits = ctypes.c_uint32(0)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().asr_take_device_error(ctypes.byref(bits), _stream_handle(dev, stream)),
                "asr_take_device_error")
     return int(bits.value)
@@ -119,7 +120,7 @@ def asr_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None, device=Non
     """Launch the bounded-wait self-test (a wait that must give up)."""
     torch = _torch()
     dev = torch.device(device if device is not None else "cuda")
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().asr_selftest_wait_timeout(int(limit_ns), _stream_handle(dev, stream)),
                "asr_selftest_wait_timeout")
 
@@ -160,6 +161,17 @@ def _dev_ptr(t, name, dtypes, numel=None):
     return t.data_ptr()
 
 
+def _on_device(device):
+    """Make ``device`` current for the call: a no-op (no device switch and
+    back) when it already is, which is the common case."""
+    torch = _torch()
+    device = torch.device(device)
+    cur = torch.cuda.current_device()
+    if device.index is None or device.index == cur:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream_handle(device, stream):
     torch = _torch()
     if stream is None:
@@ -184,7 +196,7 @@ def asr_philox4x32(out, n_ctr: int, ctr_base: int, ctr2: int, ctr3: int, seed: i
     torch = _torch()
     dts = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
     p = _dev_ptr(out, "out", dts, 4 * int(n_ctr))
-    with torch.cuda.device(out.device):
+    with _on_device(out.device):
         _check(lib().asr_philox4x32(p, int(n_ctr), int(ctr_base) & (2**64 - 1), int(ctr2) & 0xFFFFFFFF,
                                     int(ctr3) & 0xFFFFFFFF, int(seed) & (2**64 - 1),
                                     _stream_handle(out.device, stream)), "asr_philox4x32")
@@ -203,7 +215,7 @@ def asr_stochastic_round_bf16(x, out, *, base_index: int = 0, step: int = 0, see
     if rbits is not None:
         dts = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
         pr = _dev_ptr(rbits, "rbits", dts, n)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         _check(lib().asr_stochastic_round_bf16(px, pr, po, n, int(base_index), int(step) & 0xFFFFFFFF,
                                                int(seed) & (2**64 - 1), _stream_handle(x.device, stream)),
                "asr_stochastic_round_bf16")
@@ -228,7 +240,7 @@ def asr_adamw_sr_step(param, grad, exp_avg, exp_avg_sq, *, lr, beta1=0.9, beta2=
     pm = _dev_ptr(exp_avg, "exp_avg", (torch.float32,), n)
     pv = _dev_ptr(exp_avg_sq, "exp_avg_sq", (torch.float32,), n)
     h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
-    with torch.cuda.device(param.device):
+    with _on_device(param.device):
         _check(lib().asr_adamw_sr_step(pp, _dt(param), pg, _dt(grad), pm, pv, n, int(base_index),
                                        ctypes.byref(h), _stream_handle(param.device, stream)),
                "asr_adamw_sr_step")
@@ -262,7 +274,7 @@ def asr_adamw_sr_multi_tensor(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, 
         table = make_table(tensors)
         dev = tensors[0][0].device if len(tensors) else torch.device("cuda")
     h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().asr_adamw_sr_multi_tensor(table, len(table), ctypes.byref(h),
                                                _stream_handle(dev, stream)),
                "asr_adamw_sr_multi_tensor")
@@ -283,7 +295,7 @@ def asr_adamw_sr_multi_tensor_static(tensors, *, lr, beta1=0.9, beta2=0.999, eps
         table = make_table(tensors)
         dev = tensors[0][0].device if len(tensors) else torch.device("cuda")
     h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().asr_adamw_sr_multi_tensor_static(table, len(table), ctypes.byref(h),
                                                       _stream_handle(dev, stream)),
                "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr")
@@ -305,7 +317,7 @@ def asr_gemm_bf16_sr(a, b, c, c_f32=None, *, rounding="sr", step=0, seed=0, stre
     pc = _dev_ptr(c, "c", (torch.bfloat16,))
     pf = _dev_ptr(c_f32, "c_f32", (torch.float32,), m * n) if c_f32 is not None else None
     r = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE}[rounding]
-    with torch.cuda.device(a.device):
+    with _on_device(a.device):
         _check(lib().asr_gemm_bf16_sr(pa, pb, pc, pf, m, n, k, r, int(step) & 0xFFFFFFFF,
                                       int(seed) & (2**64 - 1), _stream_handle(a.device, stream)),
                "asr_gemm_bf16_sr")
