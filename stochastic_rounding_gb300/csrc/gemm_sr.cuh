@@ -437,16 +437,32 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-__device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+// The pair kernel's waits: bounded like mbar_wait (time and poll count), but
+// the timer is read only every 64 polls -- its reads sat on the path from a
+// barrier's completion to the next MMA or copy (about 1 % at 8192^3).
+template <bool CLUSTER>
+__device__ __noinline__ bool pair_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns)
 {
     const uint64_t t0 = global_ns();
-    for (uint32_t polls = 0; !mbar_test_cluster(bar, parity); ++polls) {
-        if (global_ns() - t0 > limit_ns || polls >= kWaitMaxPolls) {
+    for (uint32_t polls = 1;; ++polls) {
+        if (CLUSTER ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+        if ((polls & 63u) == 0 && (global_ns() - t0 > limit_ns || polls >= kWaitMaxPolls)) {
             atomicOr(&g_device_error, kErrWaitTimeout);
             return false;
         }
     }
-    return true;
+}
+
+__device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_test(bar, parity)) return true;
+    return pair_wait_slow<false>(bar, parity, limit_ns);
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_test_cluster(bar, parity)) return true;
+    return pair_wait_slow<true>(bar, parity, limit_ns);
 }
 
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
@@ -552,7 +568,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int s = static_cast<int>(g % kPairStages);
                 const uint32_t use = g / kPairStages;
-                if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) {
+                if (use > 0 && !pair_wait(empty(s), (use - 1) & 1u, limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -567,7 +583,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         // arrivals on its barriers have landed, before the CTA exits
         for (uint32_t s = 0; s < static_cast<uint32_t>(kPairStages) && s < g; ++s) {
             const uint32_t last_use = (g - 1 - s) / kPairStages;
-            mbar_wait(empty(static_cast<int>(s)), last_use & 1u, limit_ns);
+            pair_wait(empty(static_cast<int>(s)), last_use & 1u, limit_ns);
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
@@ -583,7 +599,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 const int s = static_cast<int>(g % kPairStages);
                 const uint32_t use = g / kPairStages;
-                if (!mbar_wait(full(s), use & 1u, limit_ns)) {
+                if (!pair_wait(full(s), use & 1u, limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -600,7 +616,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         // tensor memory or leave (also after a timeout)
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(drained)
                      : "memory");
-        mbar_wait(drained, 0, limit_ns);
+        pair_wait(drained, 0, limit_ns);
     } else if (warp >= 2) {
         // ------------------------------------------------------- epilogue
         // a warp reads the TMEM lane quarter warp % 4; with 8 warps, two
@@ -612,7 +628,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         for (uint32_t t = cluster; t < items; t += clusters, ++i) {
             const int b = static_cast<int>(i % kAccBufs);
             const uint32_t ub = i / kAccBufs;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(acc_full(b), ub & 1u, limit_ns))) break;
+            if (!__all_sync(0xFFFFFFFFu, pair_wait(acc_full(b), ub & 1u, limit_ns))) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             uint32_t m0, n0, width;
             pair_item(P, t, tiles_m, tiles_n, m0, n0, width);
