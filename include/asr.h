@@ -29,11 +29,15 @@
  *     that happen later on the GPU surface, as usual, at the next
  *     synchronising CUDA call of the caller.
  *   - n == 0 is a valid no-op (pointers may then be NULL).
- *   - Any element alignment is accepted.  16-byte-aligned buffers and a
- *     base_index that is a multiple of 4 take the vectorised fast path.
+ *   - The element-wise entry points (Philox, rounding, AdamW) accept any
+ *     element alignment; 16-byte-aligned buffers and a base_index that is a
+ *     multiple of 4 take the vectorised fast path.  The GEMM states its own
+ *     requirements.
  *   - Buffers of one call must not overlap each other (not checked).
  *   - The library is thread-safe; calls on different streams may run
  *     concurrently on disjoint buffers.
+ *   - The kernels are built for sm_103a (GB300) only; on any other GPU the
+ *     first launch fails and the call returns ASR_ERR_CUDA.
  *
  * Random bits.  Philox4x32-10 (Salmon et al., SC'11; the generator cuRAND
  * calls Philox4_32_10): multipliers 0xD2511F53 and 0xCD9E8D57, Weyl
@@ -202,9 +206,11 @@ asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_
  * (ASR_ROUND_RNE).  c_f32 (device, m x n f32, may be NULL) receives acc.
  * Requirements: n a multiple of 16, k a multiple of 8 (and k >= 8), m, n, k
  * at most 2^24, all pointers 16-byte aligned; otherwise
- * ASR_ERR_INVALID_VALUE before any launch.  m == 0 or n == 0 is a no-op.  The summation order of acc is
- * the tensor cores', so acc is reproducible run to run on one GPU model but
- * not bitwise equal to a CPU sum. */
+ * ASR_ERR_INVALID_VALUE before any launch.  m == 0 or n == 0 is a no-op.
+ * The summation order of acc is the tensor cores', so acc is reproducible
+ * run to run on one GPU model but not bitwise equal to a CPU sum.  Runs on
+ * clusters of two CTAs (tcgen05 cta_group::2) where the GPU can hold them,
+ * else on one CTA per tile; the rounding of acc is the same either way. */
 asr_status asr_gemm_bf16_sr(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, uint64_t m,
                             uint64_t n, uint64_t k, uint32_t rounding, uint32_t step, uint64_t seed,
                             asr_stream_t stream);
