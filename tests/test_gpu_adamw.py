@@ -332,3 +332,29 @@ def test_pipeline_matches_plain_path_every_step(asr, pdt, gdt, n, steps):
         assert torch.equal(ma.view(torch.int32), mb.view(torch.int32)), f"m differs at step {step}"
         assert torch.equal(va.view(torch.int32), vb.view(torch.int32)), f"v differs at step {step}"
     assert asr.asr_take_device_error() == 0
+
+
+@pytest.mark.parametrize("case", [
+    dict(lr=0.0, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=5, seed=1),
+    dict(lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8, weight_decay=0.01, step=3, seed=2),
+    dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=1, seed=3),
+    dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=2 ** 32 - 1, seed=4),
+    dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=7, seed=2 ** 64 - 1),
+], ids=["lr0", "betas0", "wd0", "step_max", "seed_max"])
+def test_degenerate_hyperparameters(asr, orc, case):
+    """The corners of the accepted hyperparameters, on both kernels (base 0
+    and base 3) with a ragged length, bit-exact against the oracle.  With
+    lr = 0 the update is p * 1 - 0, so bf16 parameters come back unchanged
+    under stochastic rounding (an exactly representable value has no bits to
+    round) while the moments still move."""
+    rng = np.random.default_rng(21)
+    n = 3 * 5120 + 13
+    for base in (0, 3):
+        h = _make(rng, n, "bf16", "bf16")
+        p0, m0 = h[0].copy(), h[2].copy()
+        d = [dev(a) for a in h]
+        _step_both(asr, orc, h, d, base_index=base, **case)
+        _check(h, d, f"{case} base={base}")
+        if case["lr"] == 0.0:
+            assert np.array_equal(host(d[0]), p0), "lr = 0 changed a bf16 parameter"
+            assert not np.array_equal(host(d[2]), m0), "lr = 0 must still update the first moment"
