@@ -132,3 +132,44 @@ def test_llama_param_set_sampled(asr, orc, shape, steps, checked):
     assert bool(torch.isfinite(ps.p[:1 << 20].float()).all())
     del ps
     torch.cuda.empty_cache()
+
+
+def test_concurrent_calls_from_threads_and_streams(asr, orc):
+    """Two host threads, each with its own stream and its own tensor set,
+    issue 5 multi-tensor steps each with no synchronisation between them (the
+    library's entry points may run concurrently on disjoint buffers): both
+    sets end bit-equal to the oracle run step by step."""
+    import threading
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    rng = np.random.default_rng(40)
+    sets = [_random_set(rng, 60, 40000), _random_set(rng, 45, 70000)]
+    devs = [_dev_set(s) for s in sets]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(k):
+        try:
+            table = _lib.make_table(devs[k])
+            for step in range(1, 6):
+                asr.asr_adamw_sr_multi_tensor(table, step=step, seed=11 + k, stream=streams[k], **HP)
+        except Exception as e:          # surfaced below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for k, host_t in enumerate(sets):
+        for (arrs, off, base), (pd, gd, md, vd, _) in zip(host_t, devs[k]):
+            p, g, m, v = (a[off:].copy() for a in arrs)
+            for step in range(1, 6):
+                orc.adamw_step(p, g, m, v, step=step, seed=11 + k, base_index=base, **HP)
+            assert_same_bits(host(pd), p, f"set {k} base {base} p")
+            assert_same_bits(host(md), m, f"set {k} base {base} m")
+            assert_same_bits(host(vd), v, f"set {k} base {base} v")
+    assert asr.asr_take_device_error() == 0
