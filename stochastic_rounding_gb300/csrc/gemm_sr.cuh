@@ -555,8 +555,11 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------- producer
-        uint32_t g = 0;
-        bool ok = true;
+        // stage s, its use count's parity, and whether every stage has been
+        // used once (only then does a stage have to be waited for)
+        uint32_t g = 0, s = 0, phase = 0;
+        bool wrapped = false, ok = true;
+        const uint32_t full0 = peer_addr(full(0), 0);       // the first CTA's barriers, 8 bytes apart
         for (uint32_t t = cluster; ok && t < items; t += clusters) {
             uint32_t m0, n0, width;
             pair_item(P, t, tiles_m, tiles_n, m0, n0, width);
@@ -565,30 +568,40 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             if (ra >= P.m) ra = 0;
             if (rb >= P.n) rb = 0;
             const uint32_t bytes = 2 * (kHalfA + (half ? kHalfB / 2 : kHalfB));
+            const CUtensorMap *mapb = half ? &map_b_half : &map_b;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
-                const int s = static_cast<int>(g % kPairStages);
-                const uint32_t use = g / kPairStages;
-                if (use > 0 && !pair_wait(empty(s), (use - 1) & 1u, limit_ns)) {
+                if (wrapped && !pair_wait(empty(s), phase ^ 1u, limit_ns)) {
                     ok = false;
                     break;
                 }
                 if (leader) mbar_arrive_expect_tx(full(s), bytes);
-                const uint32_t bar = peer_addr(full(s), 0);
+                const uint32_t bar = full0 + 8u * s;
                 const uint32_t dst = base + s * kPairStageBytes;
                 tma_load_2d_pair(dst, &map_a, kb * kBK, static_cast<int32_t>(ra), bar);
-                tma_load_2d_pair(dst + kHalfA, half ? &map_b_half : &map_b, kb * kBK, static_cast<int32_t>(rb), bar);
+                tma_load_2d_pair(dst + kHalfA, mapb, kb * kBK, static_cast<int32_t>(rb), bar);
+                if (++s == kPairStages) {
+                    s = 0;
+                    phase ^= 1u;
+                    wrapped = true;
+                }
             }
         }
         // the MMAs that read this CTA's stages have completed, and their
         // arrivals on its barriers have landed, before the CTA exits
-        for (uint32_t s = 0; s < static_cast<uint32_t>(kPairStages) && s < g; ++s) {
-            const uint32_t last_use = (g - 1 - s) / kPairStages;
-            pair_wait(empty(static_cast<int>(s)), last_use & 1u, limit_ns);
+        for (uint32_t q = 0; q < static_cast<uint32_t>(kPairStages) && q < g; ++q) {
+            const uint32_t last_use = (g - 1 - q) / kPairStages;
+            pair_wait(empty(static_cast<int>(q)), last_use & 1u, limit_ns);
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
-        uint32_t g = 0, i = 0;
+        // The tensor pipe runs only as long as this thread keeps it fed: each
+        // slice's wait, four MMAs and commit must take less than the slice's
+        // 512 MMA cycles, so descriptors advance by constants and the stage
+        // and its parity are counters (no division by the stage count).
+        uint32_t s = 0, phase = 0, i = 0;
         bool ok = true;
+        const uint64_t desc_a0 = smem_desc(base), desc_b0 = smem_desc(base + kHalfA);
+        constexpr uint64_t kDescStage = kPairStageBytes >> 4;          // a stage in descriptor address units
         for (uint32_t t = cluster; ok && t < items; t += clusters, ++i) {
             const int b = static_cast<int>(i % kAccBufs);
             const uint32_t ub = i / kAccBufs;
@@ -596,19 +609,23 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t d = tmem + static_cast<uint32_t>(b * kPairBN);
             const uint32_t idesc = t < P.wide ? kPairInstrDesc : kPairInstrDescNarrow;
-            for (int kb = 0; kb < kblocks; ++kb, ++g) {
-                const int s = static_cast<int>(g % kPairStages);
-                const uint32_t use = g / kPairStages;
-                if (!pair_wait(full(s), use & 1u, limit_ns)) {
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!pair_wait(full(s), phase, limit_ns)) {
                     ok = false;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t sa = base + s * kPairStageBytes, sb = sa + kHalfA;
-#pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_bf16_pair(d, smem_desc(sa + kk * 32), smem_desc(sb + kk * 32), idesc, (kb | kk) != 0);
+                // +2 per K=16 step: 32 bytes inside the 128-byte swizzle row
+                const uint64_t ad = desc_a0 + s * kDescStage, bd = desc_b0 + s * kDescStage;
+                mma_bf16_pair(d, ad, bd, idesc, kb != 0);
+                mma_bf16_pair(d, ad + 2, bd + 2, idesc, 1u);
+                mma_bf16_pair(d, ad + 4, bd + 4, idesc, 1u);
+                mma_bf16_pair(d, ad + 6, bd + 6, idesc, 1u);
                 mma_commit_pair(empty(s));
+                if (++s == kPairStages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
             mma_commit_pair(acc_full(b));
         }
