@@ -330,15 +330,17 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 // 0..127 of the tile in the first CTA's tensor memory and rows 128..255 in
 // the second's, all 256 columns each.  Per FLOP every SM stages and reads a
 // third less shared memory than with 128 x 256 tiles on one SM.
-//   both CTAs, warp 0 lane 0: stream the CTA's halves of A and B into a
-//       6-stage ring; the bytes of both CTAs are counted on the FIRST CTA's
+//   both CTAs, warp 0 lane 0: stream the CTA's halves of A and B, 128 deep
+//       in K (two 64-column boxes each), into a 3-stage ring of 64 KB
+//       stages; the bytes of both CTAs are counted on the FIRST CTA's
 //       "full" barrier (.cta_group::2 bulk tensor copies may signal the
 //       peer's barrier), which its producer arms with both CTAs' bytes;
 //   both CTAs, warp 1: allocate / free the tensor memory as a pair; in the
 //       first CTA its lane 0 issues the MMAs and commits them, multicast to
 //       both CTAs: each slice to the "empty" barrier of its stage (both
 //       producers wait on their own), each tile to both "acc_full" barriers;
-//   both CTAs, warps 2..5 (or 2..9): the epilogue of the CTA's 128 rows;
+//   both CTAs, warps 2..5 (2..9, 2..17 for small K): the epilogue of the
+//       CTA's 128 rows;
 //       each warp hands the accumulator back by arriving on the FIRST CTA's
 //       acc_empty barrier (2 x epilogue warps arrivals per tile).
 // A slice whose rows lie wholly past M (or N) in the second half of a tile
@@ -346,8 +348,11 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 // epilogue never stores, and no copy starts outside the matrix.
 constexpr int kPairBM = 256;                // pair tile rows: 128 per CTA
 constexpr int kPairBN = 256;                // pair tile columns: B rows, 128 staged per CTA
+#ifndef ASR_GEMM_PAIR_BK
+#define ASR_GEMM_PAIR_BK 128
+#endif
 #ifndef ASR_GEMM_PAIR_STAGES
-#define ASR_GEMM_PAIR_STAGES 6
+#define ASR_GEMM_PAIR_STAGES (ASR_GEMM_PAIR_BK == 128 ? 3 : 6)
 #endif
 #ifndef ASR_GEMM_PAIR_GROUP
 #define ASR_GEMM_PAIR_GROUP 8
@@ -366,11 +371,23 @@ struct PairShape {
     static constexpr int kThreads = 64 + 32 * EPI;     // producer warp, MMA warp, epilogue
     static constexpr int kSpan = 256 / (EPI / 4);      // columns per epilogue warp
 };
-constexpr int kPairStages = ASR_GEMM_PAIR_STAGES;   // 32 KB each: 6 fit beside the barriers, 7 just fit
+constexpr int kPairStages = ASR_GEMM_PAIR_STAGES;   // 64 KB (32 KB) stages: 3 (6) fit beside the barriers
 constexpr int kPairGroupM = ASR_GEMM_PAIR_GROUP;    // tile order: 8 pair-tile rows walked across N
 constexpr uint32_t kHalfA = 128 * kBK * 2;          // 16 KB per CTA
 constexpr uint32_t kHalfB = 128 * kBK * 2;          // 16 KB per CTA
-constexpr uint32_t kPairStageBytes = kHalfA + kHalfB;
+// K per stage: two 64-column boxes per operand, so each wait and commit of
+// the MMA thread is spread over eight MMAs (1,024 tensor cycles) instead of
+// four -- with 64 the thread's own per-slice cost (the full-barrier wait
+// ~75 cycles, four MMA issues ~280, the multicast commit ~125, measured with
+// clock64 on GB300) nearly used up the 512 cycles a slice keeps the tensor
+// pipe busy, which held it at ~79 %.  Same-run TFLOP/s at 64 / 128:
+// 8192^3 1,760-1,784 / 1,862-1,869; 4096^3 1,423-1,427 / 1,543-1,544;
+// 8192^2 x 2048 1,504-1,517 / 1,649-1,664; 16384^2 x 8192 1,815-1,819 /
+// 1,924-1,926.
+constexpr int kPairBK = ASR_GEMM_PAIR_BK;
+static_assert(kPairBK == 64 || kPairBK == 128, "K per stage: 64 or 128");
+constexpr int kPairBoxes = kPairBK / 64;
+constexpr uint32_t kPairStageBytes = kPairBoxes * (kHalfA + kHalfB);   // A boxes, then B boxes
 // barriers: full/empty per stage, full/empty per accumulator, the MMA drain
 constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + (2 * kPairStages + 2 * kAccBufs + 1) * 8 + 16;
 constexpr uint32_t pair_instr_desc(uint32_t n)
@@ -527,7 +544,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
     const uint32_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
     const uint32_t tiles_m = (P.m + kPairBM - 1) / kPairBM, tiles_n = (P.n + kPairBN - 1) / kPairBN;
     const uint32_t items = P.wide + P.narrow;
-    const int kblocks = static_cast<int>((P.k + kBK - 1) / kBK);
+    const int kblocks = static_cast<int>((P.k + kPairBK - 1) / kPairBK);   // a short last slice reads zeros past K
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairStages; ++s) {
@@ -567,7 +584,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             uint32_t ra = m0 + rank * 128, rb = n0 + rank * (width / 2);
             if (ra >= P.m) ra = 0;
             if (rb >= P.n) rb = 0;
-            const uint32_t bytes = 2 * (kHalfA + (half ? kHalfB / 2 : kHalfB));
+            const uint32_t bytes = 2 * kPairBoxes * (kHalfA + (half ? kHalfB / 2 : kHalfB));
             const CUtensorMap *mapb = half ? &map_b_half : &map_b;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
                 if (wrapped && !pair_wait(empty(s), phase ^ 1u, limit_ns)) {
@@ -577,8 +594,12 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
                 if (leader) mbar_arrive_expect_tx(full(s), bytes);
                 const uint32_t bar = full0 + 8u * s;
                 const uint32_t dst = base + s * kPairStageBytes;
-                tma_load_2d_pair(dst, &map_a, kb * kBK, static_cast<int32_t>(ra), bar);
-                tma_load_2d_pair(dst + kHalfA, mapb, kb * kBK, static_cast<int32_t>(rb), bar);
+#pragma unroll
+                for (int j = 0; j < kPairBoxes; ++j) {
+                    const int32_t x = kb * kPairBK + j * 64;
+                    tma_load_2d_pair(dst + j * kHalfA, &map_a, x, static_cast<int32_t>(ra), bar);
+                    tma_load_2d_pair(dst + kPairBoxes * kHalfA + j * kHalfB, mapb, x, static_cast<int32_t>(rb), bar);
+                }
                 if (++s == kPairStages) {
                     s = 0;
                     phase ^= 1u;
@@ -600,7 +621,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         // and its parity are counters (no division by the stage count).
         uint32_t s = 0, phase = 0, i = 0;
         bool ok = true;
-        const uint64_t desc_a0 = smem_desc(base), desc_b0 = smem_desc(base + kHalfA);
+        const uint64_t desc_a0 = smem_desc(base), desc_b0 = smem_desc(base + kPairBoxes * kHalfA);
         constexpr uint64_t kDescStage = kPairStageBytes >> 4;          // a stage in descriptor address units
         for (uint32_t t = cluster; ok && t < items; t += clusters, ++i) {
             const int b = static_cast<int>(i % kAccBufs);
@@ -615,12 +636,17 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                // +2 per K=16 step: 32 bytes inside the 128-byte swizzle row
+                // +2 per K=16 step: 32 bytes inside the 128-byte swizzle row;
+                // the next 64 columns are the next box
                 const uint64_t ad = desc_a0 + s * kDescStage, bd = desc_b0 + s * kDescStage;
-                mma_bf16_pair(d, ad, bd, idesc, kb != 0);
-                mma_bf16_pair(d, ad + 2, bd + 2, idesc, 1u);
-                mma_bf16_pair(d, ad + 4, bd + 4, idesc, 1u);
-                mma_bf16_pair(d, ad + 6, bd + 6, idesc, 1u);
+#pragma unroll
+                for (int j = 0; j < kPairBoxes; ++j) {
+                    const uint64_t aj = ad + j * (kHalfA >> 4), bj = bd + j * (kHalfB >> 4);
+                    mma_bf16_pair(d, aj, bj, idesc, (kb | j) != 0);
+                    mma_bf16_pair(d, aj + 2, bj + 2, idesc, 1u);
+                    mma_bf16_pair(d, aj + 4, bj + 4, idesc, 1u);
+                    mma_bf16_pair(d, aj + 6, bj + 6, idesc, 1u);
+                }
                 mma_commit_pair(empty(s));
                 if (++s == kPairStages) {
                     s = 0;
