@@ -348,6 +348,9 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 // epilogue never stores, and no copy starts outside the matrix.
 constexpr int kPairBM = 256;                // pair tile rows: 128 per CTA
 constexpr int kPairBN = 256;                // pair tile columns: B rows, 128 staged per CTA
+#ifndef ASR_GEMM_PDL
+#define ASR_GEMM_PDL 1               // programmatic dependent launch: overlap the prologue with the previous kernel
+#endif
 #ifndef ASR_GEMM_PAIR_BK
 #define ASR_GEMM_PAIR_BK 128
 #endif
@@ -569,6 +572,16 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
     cluster_sync();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot_ptr;
+#if ASR_GEMM_PDL
+    // Launched with programmatic stream serialization, this grid may start
+    // while the previous kernel on the stream is still finishing: everything
+    // above touches only this CTA's shared and tensor memory; global memory
+    // (A and B may be that kernel's output, C its input) waits until it has
+    // completed.  The next kernel may be launched right away -- it does the
+    // same wait before touching memory.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------- producer
@@ -797,17 +810,19 @@ asr_status launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
 {
     const unsigned clusters = pair_schedule(tiles, static_cast<uint64_t>(pairs), P);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(PairShape<EPI>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = kPairSmem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = ASR_GEMM_PDL ? 2 : 1;
     const uint64_t limit = kWaitLimitNs;
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel<EPI>, ma, mb, mb_half, P, limit);
     if (e != cudaSuccess) return cuda_fail(e);
