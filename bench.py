@@ -290,10 +290,22 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
     return out
 
 
+def step_config(n, tensors, truncated, world):
+    """The `config` of the AdamW-SR step lines (both arms)."""
+    return {"workload": ("llama3-8b" if not truncated else f"llama3-8b truncated to {n:,} params")
+                        + f": fused AdamW-SR multi-tensor step, {tensors} tensors, {n:,} params per GPU",
+            "params_per_gpu": n, "tensors": tensors,
+            "param_dtype": "bf16", "grad_dtype": "bf16", "state_dtype": "f32",
+            "rounding": "stochastic (Philox4x32-10)", "bytes_per_param": BYTES_PER_PARAM,
+            "l2": "inputs larger than L2 (176.7 GB moved per step)",
+            "parallelism": f"shard{world}" if world > 1 else "single"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    from stochastic_rounding_gb300 import workloads as W
     rates, desc = cpu_oracle_sample(args.warmup + args.steps)
     timed = rates[args.warmup:]
     value = statistics.median(timed) / 1e9
@@ -302,9 +314,10 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "llama3-8b AdamW-SR step, sampled for the CPU oracle",
-                   "params_per_step": CPU_SAMPLE_ELEMS, "param_dtype": "bf16", "grad_dtype": "bf16",
-                   "state_dtype": "f32"},
+        # the native arm's workload; each step of this arm times the oracle on
+        # a bounded sample of it (params/s is per sampled parameter)
+        "config": step_config(sum(n for _, n, _ in W.param_table(W.LLAMA_8B)), len(W.param_table(W.LLAMA_8B)),
+                              0, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -469,12 +482,7 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": ("llama3-8b" if not args.params else f"llama3-8b truncated to {n:,} params")
-                                   + f": fused AdamW-SR multi-tensor step, {len(tensors)} tensors, {n:,} params per GPU", "params_per_gpu": n, "tensors": len(tensors),
-                       "param_dtype": "bf16", "grad_dtype": "bf16", "state_dtype": "f32",
-                       "rounding": "stochastic (Philox4x32-10)", "bytes_per_param": BYTES_PER_PARAM,
-                       "l2": "inputs larger than L2 (176.7 GB moved per step)",
-                       "parallelism": f"shard{world}" if world > 1 else "single"},
+            "config": step_config(n, len(tensors), args.params, world),
             "achieved_gbs": achieved, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
