@@ -15,11 +15,17 @@
 // accumulator acc.
 //
 // C[M,N] = A[M,K] . B[N,K]^T, all row-major (both operands K-contiguous, as
-// nn.Linear keeps its weight), in 128 x 256 tiles.  Edges: the tensor maps
-// read zeros past M, N and K (zeros add nothing to the sums), and the
-// epilogue stores only rows < M and columns < N.  Persistent: one CTA per
-// SM walks the tiles in a grouped order (16 M-tiles at a time across N, so
-// the tiles in flight share operands in L2):
+// nn.Linear keeps its weight).  Two kernels compute it:
+//   gemm_bf16_sr_pair_kernel (below, used wherever the GPU can hold CTA
+//     pairs -- always on GB300): 256 x 256 tiles on clusters of two SMs with
+//     tcgen05.mma.cta_group::2, 128-deep K slices; described at its
+//     definition;
+//   gemm_bf16_sr_kernel (this one, the fallback): 128 x 256 tiles on one SM.
+// Edges, both: the tensor maps read zeros past M, N and K (zeros add nothing
+// to the sums), and the epilogue stores only rows < M and columns < N.  The
+// one-SM kernel is persistent: one CTA per SM walks the tiles in a grouped
+// order (16 M-tiles at a time across N, so the tiles in flight share
+// operands in L2):
 //   warp 0, lane 0   streams 128 x 64 and 256 x 64 slices of A and B into a
 //                    4-stage shared-memory ring (tensor-map bulk copies,
 //                    128-byte swizzle), completion counted on mbarriers;
