@@ -239,3 +239,29 @@ def test_gemm_against_oracle_gemm(asr, orc):
     same = host(acc).view(np.uint32) == want_acc.view(np.uint32)
     assert same.sum() >= 100, f"only {same.sum()} accumulators agree bitwise"
     assert np.array_equal(host(c)[same], want[same]), "same accumulator, different rounding"
+
+
+def test_gemm_special_values_in_the_epilogue(asr, orc):
+    """Inf and NaN entries in A (and products that overflow binary32) give
+    Inf / NaN accumulators; the epilogue's hardware rounding has a NaN
+    fallback, so every output -- NaN patterns included -- equals the oracle's
+    rounding of the kernel's own accumulator bit for bit (NaN: sign and top
+    payload kept, quiet bit set), SR and RNE."""
+    import torch
+    m, n, k = 200, 272, 520
+    a, b = _operands(m, n, k, seed=51)
+    a[3, 7] = float("inf")
+    a[10, 0] = float("-inf")
+    a[20, 5] = float("nan")
+    a[30, :] = 3.0e38            # row 30: products and sums overflow to +-Inf or Inf - Inf = NaN
+    a[40, 100] = float("inf")
+    b[50, 100] = 0.0             # inf * 0 = NaN in (40, 50)
+    for rounding in ("sr", "rne"):
+        c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+        acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+        asr.asr_gemm_bf16_sr(a, b, c, acc, rounding=rounding, step=2, seed=77)
+        torch.cuda.synchronize()
+        acc_h = host(acc).reshape(-1)
+        assert np.isnan(acc_h).sum() > 0 and np.isinf(acc_h).sum() > 0
+        want = orc.sr_fill(acc_h, 0, 2, 77) if rounding == "sr" else orc.rne_fill(acc_h)
+        assert_same_bits(host(c).reshape(-1), want, f"special values {rounding}", nan_equal=False)
