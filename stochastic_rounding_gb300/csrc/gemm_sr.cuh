@@ -398,7 +398,10 @@ static_assert(kPairBK == 64 || kPairBK == 128, "K per stage: 64 or 128");
 constexpr int kPairBoxes = kPairBK / 64;
 constexpr uint32_t kPairStageBytes = kPairBoxes * (kHalfA + kHalfB);   // A boxes, then B boxes
 // barriers: full/empty per stage, full/empty per accumulator, the MMA drain
-constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + (2 * kPairStages + 2 * kAccBufs + 1) * 8 + 16;
+// barriers: full per stage, empty per stage and box, full/empty per
+// accumulator, the MMA drain; then the TMEM address slot
+constexpr int kPairBars = kPairStages * (1 + kPairBoxes) + 2 * kAccBufs + 1;
+constexpr int kPairSmem = 1024 + kPairStages * kPairStageBytes + kPairBars * 8 + 16;
 constexpr uint32_t pair_instr_desc(uint32_t n)
 {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (uint32_t(kPairBM >> 4) << 24);
@@ -540,10 +543,13 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
     const uint32_t base = (raw + 1023u) & ~1023u;          // same offset in both CTAs
     const uint32_t bars = base + kPairStages * kPairStageBytes;
     auto full = [&](int s) { return bars + 8u * s; };
-    auto empty = [&](int s) { return bars + 8u * (kPairStages + s); };
-    auto acc_full = [&](int b) { return bars + 8u * (2 * kPairStages + b); };
-    auto acc_empty = [&](int b) { return bars + 8u * (2 * kPairStages + kAccBufs + b); };
-    const uint32_t drained = bars + 8u * (2 * kPairStages + 2 * kAccBufs);
+    // a stage is filled as a whole (one "full" barrier) but handed back box
+    // by box (one "empty" barrier per 64-column box): the producer can start
+    // refilling the first half while the MMAs still read the second
+    auto empty = [&](int s, int j) { return bars + 8u * (kPairStages + s * kPairBoxes + j); };
+    auto acc_full = [&](int b) { return bars + 8u * (kPairStages * (1 + kPairBoxes) + b); };
+    auto acc_empty = [&](int b) { return bars + 8u * (kPairStages * (1 + kPairBoxes) + kAccBufs + b); };
+    const uint32_t drained = bars + 8u * (kPairBars - 1);
     const uint32_t tmem_slot = drained + 8u;
     const uint32_t *tmem_slot_ptr = reinterpret_cast<const uint32_t *>(smem_raw + (tmem_slot - raw));
 
@@ -558,7 +564,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPairStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
+            for (int j = 0; j < kPairBoxes; ++j) mbar_init(empty(s, j), 1);
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(acc_full(b), 1);
@@ -606,19 +612,22 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
             const uint32_t bytes = 2 * kPairBoxes * (kHalfA + (half ? kHalfB / 2 : kHalfB));
             const CUtensorMap *mapb = half ? &map_b_half : &map_b;
             for (int kb = 0; kb < kblocks; ++kb, ++g) {
-                if (wrapped && !pair_wait(empty(s), phase ^ 1u, limit_ns)) {
-                    ok = false;
-                    break;
-                }
-                if (leader) mbar_arrive_expect_tx(full(s), bytes);
                 const uint32_t bar = full0 + 8u * s;
                 const uint32_t dst = base + s * kPairStageBytes;
 #pragma unroll
                 for (int j = 0; j < kPairBoxes; ++j) {
+                    if (wrapped && !pair_wait(empty(s, j), phase ^ 1u, limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // box 0 free means the MMAs have passed this stage's last
+                    // fill, so the full barrier is armed for the new one
+                    if (j == 0 && leader) mbar_arrive_expect_tx(full(s), bytes);
                     const int32_t x = kb * kPairBK + j * 64;
                     tma_load_2d_pair(dst + j * kHalfA, &map_a, x, static_cast<int32_t>(ra), bar);
                     tma_load_2d_pair(dst + kPairBoxes * kHalfA + j * kHalfB, mapb, x, static_cast<int32_t>(rb), bar);
                 }
+                if (!ok) break;
                 if (++s == kPairStages) {
                     s = 0;
                     phase ^= 1u;
@@ -630,7 +639,7 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
         // arrivals on its barriers have landed, before the CTA exits
         for (uint32_t q = 0; q < static_cast<uint32_t>(kPairStages) && q < g; ++q) {
             const uint32_t last_use = (g - 1 - q) / kPairStages;
-            pair_wait(empty(static_cast<int>(q)), last_use & 1u, limit_ns);
+            for (int j = 0; j < kPairBoxes; ++j) pair_wait(empty(static_cast<int>(q), j), last_use & 1u, limit_ns);
         }
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------------ MMA issuer
@@ -665,8 +674,8 @@ gemm_bf16_sr_pair_kernel(const __grid_constant__ CUtensorMap map_a, const __grid
                     mma_bf16_pair(d, aj + 2, bj + 2, idesc, 1u);
                     mma_bf16_pair(d, aj + 4, bj + 4, idesc, 1u);
                     mma_bf16_pair(d, aj + 6, bj + 6, idesc, 1u);
+                    mma_commit_pair(empty(s, j));      // this box is free once these MMAs have read it
                 }
-                mma_commit_pair(empty(s));
                 if (++s == kPairStages) {
                     s = 0;
                     phase ^= 1u;
