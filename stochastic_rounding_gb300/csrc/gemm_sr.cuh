@@ -343,7 +343,7 @@ gemm_bf16_sr_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_cons
 //       peer's barrier), which its producer arms with both CTAs' bytes;
 //   both CTAs, warp 1: allocate / free the tensor memory as a pair; in the
 //       first CTA its lane 0 issues the MMAs and commits them, multicast to
-//       both CTAs: each slice to the "empty" barrier of its stage (both
+//       both CTAs: each box of a slice to that box's "empty" barrier (both
 //       producers wait on their own), each tile to both "acc_full" barriers;
 //   both CTAs, warps 2..5 (2..9, 2..17 for small K): the epilogue of the
 //       CTA's 128 rows;
