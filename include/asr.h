@@ -205,8 +205,9 @@ asr_status asr_adamw_sr_multi_tensor_static(const asr_tensor_desc *table, int32_
  * (seed, step) (rounding = ASR_ROUND_SR), or to nearest-even
  * (ASR_ROUND_RNE).  c_f32 (device, m x n f32, may be NULL) receives acc.
  * Requirements: n a multiple of 16, k a multiple of 8 (and k >= 8), m, n, k
- * at most 2^24, all pointers 16-byte aligned; otherwise
- * ASR_ERR_INVALID_VALUE before any launch.  m == 0 or n == 0 is a no-op.
+ * at most 2^24, fewer than 2^31 output tiles (ceil(m/256) * ceil(n/256)),
+ * all pointers 16-byte aligned; otherwise ASR_ERR_INVALID_VALUE before any
+ * launch.  m == 0 or n == 0 is a no-op.
  * The summation order of acc is the tensor cores', so acc is reproducible
  * run to run on one GPU model but not bitwise equal to a CPU sum.  Runs on
  * clusters of two CTAs (tcgen05 cta_group::2) where the GPU can hold them,
