@@ -868,6 +868,9 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (!a || !b || !c) return ASR_ERR_INVALID_VALUE;
     if (n % 16 || k == 0 || k % 8) return ASR_ERR_INVALID_VALUE;
     if (m > (1u << 24) || n > (1u << 24) || k > (1u << 24)) return ASR_ERR_INVALID_VALUE;
+    // the tile index is 32-bit: checked here, before any CUDA call, on the
+    // larger two-SM tiles (the one-SM fallback's own count is checked later)
+    if (((m + 255) / 256) * ((n + 255) / 256) >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(c) || (c_f32 && !aligned16(c_f32)))
         return ASR_ERR_INVALID_VALUE;
     int sms = 0, pairs[3] = {0, 0, 0};

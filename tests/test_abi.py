@@ -155,7 +155,8 @@ def test_gemm_rejects_bad_shapes_before_launching(L):
     call (no GPU needed)."""
     p = ctypes.c_void_p(4096)
     g = L.asr_gemm_bf16_sr
-    for m, n, k in ((128, 100, 64), (128, 136, 64 + 4), (128, 128, 0), (1 << 25, 128, 64), (128, 1 << 25, 64)):
+    for m, n, k in ((128, 100, 64), (128, 136, 64 + 4), (128, 128, 0), (1 << 25, 128, 64), (128, 1 << 25, 64),
+                    (1 << 24, 1 << 24, 64)):     # the last: within each limit, but 2^32 output tiles
         assert g(p, p, p, None, m, n, k, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE, (m, n, k)
     assert g(None, p, p, None, 128, 128, 64, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE
     assert g(ctypes.c_void_p(4097), p, p, None, 128, 128, 64, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE
