@@ -35,7 +35,9 @@
  *     requirements.
  *   - Buffers of one call must not overlap each other (not checked).
  *   - The library is thread-safe; calls on different streams may run
- *     concurrently on disjoint buffers.
+ *     concurrently on disjoint buffers.  One exception:
+ *     asr_adamw_sr_multi_tensor_static keeps its table in one shared device
+ *     array, so its calls must not overlap one another on the GPU.
  *   - The kernels are built for sm_103a (GB300) only; on any other GPU the
  *     first launch fails and the call returns ASR_ERR_CUDA.
  *
@@ -184,8 +186,11 @@ asr_status asr_adamw_sr_multi_tensor(const asr_tensor_desc *table, int32_t n_ten
  *     device address, via cudaGetSymbolAddress with the device current, and
  *     the kernels' launch shapes); make that first call before any stream
  *     capture.
- *   - The table is copied from host memory on `stream`, so the call returns
- *     only after the work already queued on `stream` has finished.
+ *   - The table is copied into the array from the library's (pageable)
+ *     host staging buffer with an asynchronous copy on `stream`: the runtime
+ *     has taken the host bytes by the time the call returns, and the copy is
+ *     ordered after earlier work on `stream` and before the kernels that
+ *     read it.  The call does not wait for the GPU.
  *   - Every call reuses the one array and leaves its table there: calls whose
  *     kernels overlap on the GPU (other streams, other host threads) race on
  *     it.  Each call rewrites the part it uses; nothing has to start at zero. */

@@ -80,7 +80,7 @@ def lib() -> ctypes.CDLL:
         L.asr_gemm_bf16_sr.restype = ctypes.c_int
         for f in ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
                   "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor",
-                  "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr"):
+                  "asr_adamw_sr_multi_tensor_static"):
             getattr(L, f).restype = ctypes.c_int
         L.asr_status_string.argtypes = [ctypes.c_int]
         L.asr_status_string.restype = ctypes.c_char_p
@@ -298,7 +298,7 @@ def asr_adamw_sr_multi_tensor_static(tensors, *, lr, beta1=0.9, beta2=0.999, eps
     with _on_device(dev):
         _check(lib().asr_adamw_sr_multi_tensor_static(table, len(table), ctypes.byref(h),
                                                       _stream_handle(dev, stream)),
-               "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr")
+               "asr_adamw_sr_multi_tensor_static")
 
 
 def asr_gemm_bf16_sr(a, b, c, c_f32=None, *, rounding="sr", step=0, seed=0, stream=None):

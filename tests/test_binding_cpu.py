@@ -1,0 +1,70 @@
+"""The multi-tensor wrappers of the binding against a stand-in library (no
+GPU): one C call per wrapper call, None on success, AsrError carrying the
+status otherwise -- never an exception after a call that succeeded, which
+would invite a caller to retry and apply the step twice."""
+import contextlib
+import ctypes
+
+import pytest
+
+from stochastic_rounding_gb300 import _lib
+
+NAMES = ("asr_adamw_sr_multi_tensor", "asr_adamw_sr_multi_tensor_static")
+
+
+class _StubLib:
+    def __init__(self, status):
+        self.status = status
+        self.calls = {n: 0 for n in NAMES}
+
+    def __getattr__(self, name):
+        if name in NAMES:
+            def call(table, n, hp, stream):
+                self.calls[name] += 1
+                assert n == len(table) and hp._obj.step == 3
+                return self.status
+            return call
+        raise AttributeError(name)
+
+    @staticmethod
+    def asr_status_string(s):
+        return b"ASR_STATUS_%d" % s
+
+    @staticmethod
+    def asr_last_cuda_error():
+        return 0
+
+
+@pytest.fixture
+def stub(monkeypatch):
+    def make(status):
+        s = _StubLib(status)
+        monkeypatch.setattr(_lib, "_lib", s)
+        monkeypatch.setattr(_lib, "_on_device", lambda d: contextlib.nullcontext())
+        monkeypatch.setattr(_lib, "_stream_handle", lambda d, s: ctypes.c_void_p(None))
+        return s
+    return make
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_wrapper_returns_once_on_success(stub, name):
+    s = stub(_lib.ASR_OK)
+    table = (_lib.TensorDesc * 3)()
+    assert getattr(_lib, name)(table, lr=1e-3, step=3, device="cpu") is None
+    assert s.calls[name] == 1
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_wrapper_raises_the_status(stub, name):
+    s = stub(_lib.ASR_ERR_INVALID_VALUE)
+    table = (_lib.TensorDesc * 2)()
+    with pytest.raises(_lib.AsrError) as e:
+        getattr(_lib, name)(table, lr=1e-3, step=3, device="cpu")
+    assert e.value.status == _lib.ASR_ERR_INVALID_VALUE and name in str(e.value)
+    assert s.calls[name] == 1
+
+
+def test_package_exports_both_wrappers():
+    import stochastic_rounding_gb300 as asr
+    for name in NAMES:
+        assert getattr(asr, name) is getattr(_lib, name)
