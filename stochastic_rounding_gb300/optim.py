@@ -8,17 +8,39 @@ bfloat16.  Section Method: the rounding bits are keyed by (seed, step) and
 indexed by each element's global parameter position.
 
 Global positions: the parameters, in the order the optimizer was given them
-(all groups, in group order), are laid end to end; a parameter's base index
-is the number of elements before it.  Every step of a group is one
-multi-tensor launch (per device and per distinct step count).
+(all groups, in group order), are laid end to end from ``base_offset``; a
+parameter's base index is ``base_offset`` plus the number of elements before
+it.  A group may instead name the position of its first element with a
+``base_index`` key (its later parameters follow on from there, and so does
+the next group).  An optimizer that holds one rank's contiguous share of a
+model's flat parameter vector therefore passes the share's start as
+``base_offset`` and draws exactly the bits the whole-model update would
+(section Method: identical whether a parameter is updated whole or split
+across shards and ranks).  Every step of a group is one multi-tensor launch
+(per device and per distinct step count).
+
+Device errors: the kernels' pipeline waits give up after a time limit rather
+than hang, leaving the step incomplete and raising a sticky device error bit.
+With ``check_errors`` (the default) every ``step()`` reads that bit once its
+launches are queued, which waits for the step to finish on the device (one
+host synchronisation per step), and raises ``DeviceError`` if it is set.
+``check_errors=False`` skips the read (no synchronisation); the caller then
+checks with ``stochastic_rounding_gb300.asr_take_device_error`` when it
+wants to.
 """
 from __future__ import annotations
 
-from typing import Dict, List
+from typing import Dict, List, Optional
 
 import torch
 
 from . import _lib
+
+
+class DeviceError(RuntimeError):
+    """A kernel of the step reported a device error (a pipeline wait that
+    gave up): the step was not completed on every element, so parameters
+    and moments are partly updated and should be restored from a checkpoint."""
 
 
 class AdamWSR(torch.optim.Optimizer):
@@ -27,12 +49,15 @@ class AdamWSR(torch.optim.Optimizer):
     Arguments follow ``torch.optim.AdamW`` (``lr``, ``betas``, ``eps``,
     ``weight_decay``) plus ``seed`` (64-bit key of the rounding stream) and
     ``rounding`` (``"sr"``, or ``"rne"`` for round-to-nearest-even, the
-    biased baseline).  Parameters must be contiguous CUDA tensors of float32
+    biased baseline), ``base_offset`` (global position of the first
+    parameter's element 0) and ``check_errors`` (read the device error bit
+    after every step).  Parameters must be contiguous CUDA tensors of float32
     or bfloat16; gradients dense float32 or bfloat16.
     """
 
     def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
-                 weight_decay: float = 1e-2, *, seed: int = 0, rounding: str = "sr"):
+                 weight_decay: float = 1e-2, *, seed: int = 0, rounding: str = "sr",
+                 base_offset: int = 0, check_errors: bool = True):
         if not 0.0 <= lr:
             raise ValueError(f"Invalid learning rate: {lr}")
         if not 0.0 <= eps:
@@ -47,19 +72,29 @@ class AdamWSR(torch.optim.Optimizer):
             raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")
         if not 0 <= int(seed) < 2**64:
             raise ValueError("seed must fit in 64 bits")
+        if not 0 <= int(base_offset) < 2**64:
+            raise ValueError("base_offset must fit in 64 bits")
+        self.base_offset = int(base_offset)
+        self.check_errors = bool(check_errors)
         defaults = dict(lr=lr, betas=tuple(betas), eps=eps, weight_decay=weight_decay,
-                        seed=int(seed), rounding=rounding)
+                        seed=int(seed), rounding=rounding, base_index=None)
         super().__init__(params, defaults)
         self._assign_positions()
         self._table_cache: Dict[tuple, object] = {}
 
     def _assign_positions(self):
-        pos = 0
+        pos = self.base_offset
         self._base: Dict[int, int] = {}
         for group in self.param_groups:
+            if group.get("base_index") is not None:
+                if not 0 <= int(group["base_index"]) < 2**64:
+                    raise ValueError("a group's base_index must fit in 64 bits")
+                pos = int(group["base_index"])
             for p in group["params"]:
                 if id(p) in self._base:
                     continue
+                if pos + p.numel() > 2**64:
+                    raise ValueError("global positions run past 2^64")
                 self._base[id(p)] = pos
                 pos += p.numel()
 
@@ -89,11 +124,14 @@ class AdamWSR(torch.optim.Optimizer):
             raise ValueError("gradient must be contiguous, on the parameter's device and of its shape")
 
     @torch.no_grad()
-    def step(self, closure=None):
+    def step(self, closure=None, *, check_errors: Optional[bool] = None):
+        """One AdamW-SR step of every parameter that has a gradient.
+        ``check_errors`` overrides the optimizer's setting for this call."""
         loss = None
         if closure is not None:
             with torch.enable_grad():
                 loss = closure()
+        devices = set()
         for group in self.param_groups:
             beta1, beta2 = group["betas"]
             # (device, step) -> list of (p, g, m, v, base)
@@ -119,6 +157,13 @@ class AdamWSR(torch.optim.Optimizer):
                     table, lr=group["lr"], beta1=beta1, beta2=beta2, eps=group["eps"],
                     weight_decay=group["weight_decay"], step=step, seed=group["seed"],
                     rounding=group["rounding"], device=device)
+                devices.add(device)
+        if self.check_errors if check_errors is None else check_errors:
+            for device in devices:
+                bits = _lib.asr_take_device_error(device=device)
+                if bits:
+                    raise DeviceError(f"AdamWSR.step: device error bits {bits:#x} on {device} "
+                                      "(a pipeline wait gave up; the step is incomplete)")
         return loss
 
     def _table(self, entries):
@@ -150,4 +195,7 @@ class AdamWSR(torch.optim.Optimizer):
                     self.state[p][k] = st[k].to(device=p.device, dtype=torch.float32, copy=True)
             if "step" in self.state[p]:
                 self.state[p]["step"] = int(self.state[p]["step"])
+        for group in self.param_groups:
+            group.setdefault("base_index", None)
+        self._assign_positions()
         self._table_cache.clear()

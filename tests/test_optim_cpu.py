@@ -26,3 +26,77 @@ def test_cpu_parameters_are_refused():
     opt = AdamWSR([p])
     with pytest.raises(ValueError, match="CUDA"):
         opt.step()
+
+
+def test_base_offset_and_group_base_index():
+    ps = [torch.nn.Parameter(torch.zeros(s)) for s in (3, 5, 7, 2)]
+    opt = AdamWSR([{"params": ps[:2]}, {"params": ps[2:3], "base_index": 1000}, {"params": ps[3:]}],
+                  base_offset=2**40 + 1)
+    assert [opt.base_index(p) for p in ps] == [2**40 + 1, 2**40 + 4, 1000, 1007]
+    opt.add_param_group({"params": [torch.nn.Parameter(torch.zeros(4))], "base_index": 5})
+    assert opt.base_index(opt.param_groups[-1]["params"][0]) == 5
+    with pytest.raises(ValueError):
+        AdamWSR(ps, base_offset=-1)
+    with pytest.raises(ValueError):
+        AdamWSR([torch.nn.Parameter(torch.zeros(8))], base_offset=2**64 - 4)
+
+
+def test_positions_survive_a_state_dict_round_trip():
+    ps = [torch.nn.Parameter(torch.zeros(s)) for s in (3, 5)]
+    a = AdamWSR([{"params": ps[:1]}, {"params": ps[1:], "base_index": 77}], base_offset=9)
+    qs = [torch.nn.Parameter(torch.zeros(s)) for s in (3, 5)]
+    b = AdamWSR([{"params": qs[:1]}, {"params": qs[1:]}], base_offset=9)
+    assert b.base_index(qs[1]) == 12
+    b.load_state_dict(a.state_dict())
+    assert [b.base_index(q) for q in qs] == [a.base_index(p) for p in ps] == [9, 77]
+
+
+class _FakeLib:
+    """Stands in for the binding: records launches, reports set error bits."""
+
+    def __init__(self, bits):
+        self.bits = bits
+        self.calls = []
+        self.reads = 0
+
+    def make_table(self, entries):
+        return [e[4] for e in entries]
+
+    def asr_adamw_sr_multi_tensor(self, table, **kw):
+        self.calls.append((list(table), kw["step"]))
+
+    def asr_take_device_error(self, device=None):
+        self.reads += 1
+        return self.bits
+
+
+def _fake_step(monkeypatch, bits, **kw):
+    from stochastic_rounding_gb300 import optim
+    fake = _FakeLib(bits)
+    monkeypatch.setattr(optim, "_lib", fake)
+    monkeypatch.setattr(AdamWSR, "_check", staticmethod(lambda p: None))
+    ps = [torch.nn.Parameter(torch.zeros(s)) for s in (4, 6)]
+    for p in ps:
+        p.grad = torch.zeros_like(p)
+    opt = AdamWSR(ps, base_offset=100, **kw)
+    return opt, fake
+
+
+def test_step_raises_when_a_kernel_reported_a_device_error(monkeypatch):
+    from stochastic_rounding_gb300.optim import DeviceError
+    opt, fake = _fake_step(monkeypatch, 1)
+    with pytest.raises(DeviceError, match="0x1"):
+        opt.step()
+    assert fake.calls == [([100, 104], 1)] and fake.reads == 1
+    opt.step(check_errors=False)              # per-call override: no read
+    assert fake.reads == 1
+
+
+def test_step_without_error_checks_reads_nothing(monkeypatch):
+    opt, fake = _fake_step(monkeypatch, 1, check_errors=False)
+    opt.step()
+    opt.step()
+    assert fake.reads == 0 and [s for _, s in fake.calls] == [1, 2]
+    fake.bits = 0
+    opt.step(check_errors=True)               # clean word: no exception
+    assert fake.reads == 1
