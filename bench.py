@@ -44,6 +44,18 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CPU_SAMPLE_ELEMS = 1 << 24     # oracle sample per step (one core)
 
 
+def require_no_device_error(take_error, region):
+    """Read (and clear) the library's device error word after a timed region,
+    outside it.  A set bit means a kernel's pipeline wait gave up and left
+    work undone, which would make the step look faster than it is: the
+    benchmark then stops with a non-zero exit and prints no result line."""
+    bits = take_error()
+    if bits:
+        print(f"bench.py: device error bits {bits:#x} after the {region}: a kernel left work undone; "
+              "no result is reported", file=sys.stderr, flush=True)
+        raise SystemExit(3)
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
@@ -176,6 +188,50 @@ def cpu_oracle_sample(steps, sample_elems=CPU_SAMPLE_ELEMS, seed=0):
     return rates, desc
 
 
+def host_link_rates(dev, nbytes=1 << 30, reps=3):
+    """GB/s of this machine's host link with page-locked host memory, measured
+    outside the timed steps: one nbytes host-to-device copy, one
+    device-to-host copy, and one of each at once on two streams (aggregate
+    bytes / time); best of ``reps`` each, CUDA events."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s1)
+            s2.wait_stream(s1)
+            fn()
+            s1.wait_stream(s2)
+            e1.record(s1)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+    rates = {"h2d": nbytes / (timed(h2d) / 1e3) / 1e9, "d2h": nbytes / (timed(d2h) / 1e3) / 1e9,
+             "both": 2 * nbytes / (timed(both) / 1e3) / 1e9}
+    del h_in, h_out, d_in, d_out
+    return rates
+
+
 def e2e_chunks(tensors, offset, max_params=1 << 28):
     """Consecutive tensors grouped into chunks of at most max_params (a larger
     tensor is a chunk of its own).  Each chunk is a contiguous range [lo, hi)
@@ -275,6 +331,7 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
 
     single("single_65536_bf16", 65536, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM,
            "1.4 MB: L2-resident and launch-bound")
+    out["single_65536_bf16"]["host_us_per_call"] = binding_host_cost(asr, W, dev, gen)
     single("fp32_16777216", 16777216, torch.float32, torch.float32, 28, "fp32 params and grads")
     single("bf16_268435456", 268435456, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM, "one tensor")
     ps = W.DeviceParamSet(W.LLAMA_1B, device=dev, seed=2)
@@ -287,7 +344,49 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
                                    "frac_of_measured_copy": gbs / peak, "note": "147 tensors, one launch"}
     del ps
     torch.cuda.empty_cache()
+    # the stand-alone kernels of the library, each a few seconds at most
+    for m, n, k, budget in ((8192, 8192, 8192, 1e9), (8192, 8192, 1024, 2.5e8), (8192, 8192, 512, 2.5e8)):
+        out[f"gemm_{m}x{n}x{k}"] = gemm_measure(asr, dev, m, n, k, steps, warmup, budget)
+    out["sr_op_1073741824"] = elementwise_measure(asr, dev, "sr", 1 << 30, steps, warmup)
+    out["philox_268435456"] = elementwise_measure(asr, dev, "philox", 1 << 28, steps, warmup)
+    torch.cuda.empty_cache()
     return out
+
+
+def binding_host_cost(asr, W, dev, gen, n=65536, calls=200):
+    """Host time per call (microseconds) to enqueue one single-tensor step:
+    through the C ABI directly (ctypes, arguments marshalled once) and
+    through the Python binding (tensor checks, hyperparameter struct, stream
+    lookup every call).  Few enough calls that the launch queue never fills,
+    so the host loop is not held up by the GPU."""
+    import ctypes
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    p = W.device_normal_(torch.empty(n, dtype=torch.bfloat16, device=dev), gen, 0.02)
+    g = W.device_normal_(torch.empty(n, dtype=torch.bfloat16, device=dev), gen, 1e-3)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    L = _lib.lib()
+    sh = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    hps = [_lib.make_hparams(step=t, seed=0, **HP) for t in range(1, calls + 1)]
+    args = (ctypes.c_void_p(p.data_ptr()), _lib.ASR_BF16, ctypes.c_void_p(g.data_ptr()), _lib.ASR_BF16,
+            ctypes.c_void_p(m.data_ptr()), ctypes.c_void_p(v.data_ptr()), n, 0)
+    res = {}
+    for rep in range(2):                     # the first pass warms both paths up
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for h in hps:
+            if L.asr_adamw_sr_step(*args, ctypes.byref(h), sh) != _lib.ASR_OK:
+                raise RuntimeError("asr_adamw_sr_step failed")
+        res["c_abi"] = (time.perf_counter() - t0) / calls * 1e6
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for t in range(1, calls + 1):
+            asr.asr_adamw_sr_step(p, g, m, v, step=t, seed=0, **HP)
+        res["python_binding"] = (time.perf_counter() - t0) / calls * 1e6
+        torch.cuda.synchronize(dev)
+    require_no_device_error(asr.asr_take_device_error, "binding cost calls")
+    return res
 
 
 def step_config(n, tensors, truncated, world):
@@ -371,6 +470,7 @@ def run_gpu(args):
         t_global += 1
         step(t_global)
     torch.cuda.synchronize(dev)
+    require_no_device_error(asr.asr_take_device_error, "warm-up steps")
 
     # ---- device-resident timed region
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -389,6 +489,7 @@ def run_gpu(args):
         all_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier()
+    require_no_device_error(asr.asr_take_device_error, "timed device-resident steps")
     total_ms = max_over_ranks(all_start.elapsed_time(all_end))
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     launch_ms = statistics.mean(per_launch_ms)
@@ -461,9 +562,13 @@ def run_gpu(args):
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
+    require_no_device_error(asr.asr_take_device_error, "timed end-to-end steps")
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
     del g_host, p_host
+    link = host_link_rates(dev)
+    # the copies alone bound the end-to-end step: 2n bytes in and 2n out
+    floor_s = max(2 * n / (link["h2d"] * 1e9), 2 * n / (link["d2h"] * 1e9), 4 * n / (link["both"] * 1e9))
 
     others = None
     if rank == 0 and not args.params:
@@ -493,6 +598,8 @@ def run_gpu(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * n,
                     "d2h_bytes_per_step": 2 * n, "steps": e_steps, "chunks": len(chunks),
                     "gpu_launches": launches_e2e,
+                    "link_gbs": link, "link_floor_gparams_s": n / floor_s / 1e9,
+                    "frac_of_link_floor": e2e_value / world / (n / floor_s / 1e9),
                     "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host; "
                             "chunks of consecutive tensors pipelined over three streams"},
             "gpu_launches": launches,
@@ -524,118 +631,171 @@ def gemm_cpu_baseline(a, b, m, n, k, budget_macs=6e9):
             "sample": f"{rows} of {m} rows x {n} columns x K={k}, C oracle single thread, {dt:.1f} s"}
 
 
-def run_gemm(args):
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+# The SR epilogue's integer-multiply ceiling.  Each output element takes a
+# quarter of a Philox4x32-10 call: 10 rounds x 2 products (32 x 32 -> 64 bits)
+# / 4 outputs = 5 products, i.e. 10 32-bit multiply results (low and high
+# halves).  The public CUDA throughput table gives 64 32-bit integer
+# multiply(-add) results per clock per SM.
+EPILOGUE_MUL_RESULTS_PER_OUTPUT = 10
+INT_MUL_RESULTS_PER_CLK_PER_SM = 64
+
+
+def gemm_measure(asr, dev, m, n, k, steps, warmup, cpu_budget_macs):
     """The tcgen05 GEMM with the stochastic-rounding epilogue (and with the
     round-to-nearest epilogue, and torch.matmul = cuBLAS, for context) on
     one m x n x k problem: TFLOP/s by CUDA events over the timed launches,
-    against the measured bf16 tensor peak."""
+    against the measured bf16 tensor peak; beside it the epilogue's
+    integer-multiply rate against the SMs' integer-multiply ceiling at the
+    maximum SM clock (the bound that matters at small K)."""
     import torch
-    from __graft_entry__ import build
-    build()
-    import stochastic_rounding_gb300 as asr
-    m, n, k = args.gemm
-    dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(0)
     a = torch.randn(m, k, device=dev, generator=g).to(torch.bfloat16)
     b = torch.randn(n, k, device=dev, generator=g).to(torch.bfloat16)
     c = torch.empty(m, n, device=dev, dtype=torch.bfloat16)
     flops = 2.0 * m * n * k
+    stream = torch.cuda.current_stream(dev)
 
     def timed(fn):
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             fn()
-        torch.cuda.synchronize()
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
+        e0.record(stream)
+        for _ in range(steps):
             fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / args.steps
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
 
     t_sr = timed(lambda: asr.asr_gemm_bf16_sr(a, b, c, rounding="sr", step=1, seed=0))
     t_rn = timed(lambda: asr.asr_gemm_bf16_sr(a, b, c, rounding="rne"))
+    require_no_device_error(asr.asr_take_device_error, f"timed GEMM {m}x{n}x{k}")
     t_cublas = timed(lambda: torch.matmul(a, b.t()))
+    peak, kind = bf16_peak()
+    tf = flops / (t_sr / 1e3) / 1e12
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peak, kind = float(json.load(f)["bf16_tflops"]), "measured"
+            clk_mhz = float(json.load(f)["sm_max_mhz"])
     except Exception:
-        peak, kind = 1900.0, "fallback"
-    tf = flops / (t_sr / 1e3) / 1e12
-    cpu = gemm_cpu_baseline(a, b, m, n, k)
-    line = {"metric": "bf16 GEMM with stochastic-rounding epilogue TFLOP/s", "value": tf, "unit": "TFLOP/s",
-            "ms": t_sr, "config": {"workload": f"gemm {m}x{n}x{k} bf16, f32 accumulate, C = A.B^T"},
-            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
-                         "peak_kind": kind},
-            "rne_epilogue_tflops": flops / (t_rn / 1e3) / 1e12,
-            "cublas_torch_matmul_tflops": flops / (t_cublas / 1e3) / 1e12,
-            "cpu_baseline": cpu,
-            "steps": args.steps, "warmup": args.warmup}
-    print(json.dumps(line), flush=True)
-    return 0
+        clk_mhz = 2070.0
+    mul_rate = EPILOGUE_MUL_RESULTS_PER_OUTPUT * m * n / (t_sr / 1e3)
+    mul_peak = sms * clk_mhz * 1e6 * INT_MUL_RESULTS_PER_CLK_PER_SM
+    entry = {"workload": f"gemm {m}x{n}x{k} bf16, f32 accumulate, C = A.B^T, SR epilogue",
+             "ms": t_sr, "tflops": tf,
+             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                          "peak_kind": kind},
+             "epilogue_int_mul": {"achieved": mul_rate / 1e12, "peak": mul_peak / 1e12,
+                                  "unit": "T multiply results/s", "frac": mul_rate / mul_peak,
+                                  "per_output": EPILOGUE_MUL_RESULTS_PER_OUTPUT,
+                                  "peak_basis": f"{sms} SMs x {clk_mhz:.0f} MHz x "
+                                                f"{INT_MUL_RESULTS_PER_CLK_PER_SM}/clk/SM"},
+             "rne_epilogue_tflops": flops / (t_rn / 1e3) / 1e12,
+             "cublas_torch_matmul_tflops": flops / (t_cublas / 1e3) / 1e12,
+             "steps": steps, "warmup": warmup}
+    if cpu_budget_macs:
+        entry["cpu_baseline"] = gemm_cpu_baseline(a, b, m, n, k, cpu_budget_macs)
+    del a, b, c
+    return entry
 
 
-def run_elementwise(args):
-    """The stand-alone rounding op (--sr N: float32 -> bf16 with Philox bits,
-    6 B per element) or the Philox op (--philox N: N counters, 16 B written
-    each) over N elements resident in HBM (larger than L2), by CUDA events
-    over the timed launches, against the measured copy bandwidth; the oracle
-    on a 2^22-element sample beside it."""
-    import numpy as np
+def run_gemm(args):
+    """One GEMM problem (--gemm M N K) as its own JSON line."""
     import torch
     from __graft_entry__ import build
     build()
     import stochastic_rounding_gb300 as asr
-    import oracle
+    m, n, k = args.gemm
     dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    if args.sr:
-        n, unit_bytes, what = args.sr, 6, "stand-alone stochastic rounding float32 -> bf16"
+    e = gemm_measure(asr, dev, m, n, k, args.steps, args.warmup, 6e9)
+    line = {"metric": "bf16 GEMM with stochastic-rounding epilogue TFLOP/s", "value": e["tflops"],
+            "unit": "TFLOP/s", "ms": e["ms"], "config": {"workload": e["workload"]},
+            "roofline": e["roofline"], "epilogue_int_mul": e["epilogue_int_mul"],
+            "rne_epilogue_tflops": e["rne_epilogue_tflops"],
+            "cublas_torch_matmul_tflops": e["cublas_torch_matmul_tflops"],
+            "cpu_baseline": e["cpu_baseline"], "steps": args.steps, "warmup": args.warmup}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def elementwise_measure(asr, dev, kind, n, steps, warmup, sample=1 << 22):
+    """The stand-alone rounding op (kind "sr": float32 -> bf16 with Philox
+    bits, 6 B per element) or the Philox op (kind "philox": n counters, 16 B
+    written each) over n elements resident in HBM (larger than L2), by CUDA
+    events over the timed launches, against the measured copy bandwidth; the
+    oracle on a ``sample``-element sample beside it."""
+    import torch
+    import oracle
+    if kind == "sr":
+        unit_bytes, what = 6, "stand-alone stochastic rounding float32 -> bf16"
         g = torch.Generator(device=dev)
         g.manual_seed(0)
         x = torch.randn(n, device=dev, generator=g)
         out = torch.empty(n, device=dev, dtype=torch.bfloat16)
-        fn = lambda: asr.asr_stochastic_round_bf16(x, out, base_index=0, step=1, seed=0)
+        fn = lambda: asr.asr_stochastic_round_bf16(x, out, base_index=0, step=1, seed=0)  # noqa: E731
     else:
-        n, unit_bytes, what = args.philox, 16, "Philox4x32-10 counters, four words each"
+        unit_bytes, what = 16, "Philox4x32-10 counters, four words each"
+        x = None
         out = torch.empty(4 * n, device=dev, dtype=torch.int32)
-        fn = lambda: asr.asr_philox4x32(out, n, 0, 1, 0, 0)
-    for _ in range(args.warmup):
+        fn = lambda: asr.asr_philox4x32(out, n, 0, 1, 0, 0)  # noqa: E731
+    for _ in range(warmup):
         fn()
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         fn()
     e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    err = asr.asr_take_device_error()
-    if err:
-        raise RuntimeError(f"device error word {err:#x}")
-    peak, kind = measured_peak()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    require_no_device_error(asr.asr_take_device_error, f"timed {kind} launches")
+    peak, pkind = measured_peak()
     gbs = unit_bytes * n / (ms / 1e3) / 1e9
     o = oracle.get()
-    sample = 1 << 22
     t0 = time.perf_counter()
-    if args.sr:
+    if kind == "sr":
         o.sr_fill(x[:sample].cpu().numpy(), 0, 1, 0)
     else:
         o.philox_fill(sample, 0, 1, 0, 0)
     dt = time.perf_counter() - t0
-    unit = "Gelem/s" if args.sr else "Gctr/s"
-    line = {"metric": f"{what} {unit}", "value": n / (ms / 1e3) / 1e9, "unit": unit, "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "dtype": "f32->bf16" if args.sr else "u32", "data": "synthetic",
-            "config": {"workload": f"{what}, {n:,} {'elements' if args.sr else 'counters'}",
-                       "l2": "inputs and outputs larger than L2"},
+    unit = "Gelem/s" if kind == "sr" else "Gctr/s"
+    del x, out
+    return {"workload": f"{what}, {n:,} {'elements' if kind == 'sr' else 'counters'}", "what": what,
+            "value": n / (ms / 1e3) / 1e9, "unit": unit, "ms": ms,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                         "peak_kind": kind, "bytes_per_unit": unit_bytes},
+                         "peak_kind": pkind, "bytes_per_unit": unit_bytes},
             "cpu_baseline": {"value": sample / dt / 1e9, "unit": unit, "cores": 1, "kind": "oracle",
-                             "sample": f"{sample:,} {'elements' if args.sr else 'counters'}, C oracle single thread"},
-            "gpu_launches": args.steps}
+                             "sample": f"{sample:,} {'elements' if kind == 'sr' else 'counters'}, "
+                                       f"C oracle single thread"},
+            "steps": steps, "warmup": warmup}
+
+
+def run_elementwise(args):
+    """The stand-alone rounding op (--sr N) or the Philox op (--philox N) as
+    its own JSON line."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    import stochastic_rounding_gb300 as asr
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kind, n = ("sr", args.sr) if args.sr else ("philox", args.philox)
+    e = elementwise_measure(asr, dev, kind, n, args.steps, args.warmup)
+    line = {"metric": f"{e['what']} {e['unit']}", "value": e["value"], "unit": e["unit"], "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": e["ms"], "higher_is_better": True,
+            "dtype": "f32->bf16" if kind == "sr" else "u32", "data": "synthetic",
+            "config": {"workload": e["workload"], "l2": "inputs and outputs larger than L2"},
+            "roofline": e["roofline"], "cpu_baseline": e["cpu_baseline"], "gpu_launches": args.steps}
     print(json.dumps(line), flush=True)
     return 0
 

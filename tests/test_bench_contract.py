@@ -23,3 +23,36 @@ def test_reference_arm_line():
     assert d["config"]["params_per_gpu"] == 8_030_261_248 and d["config"]["tensors"] == 291
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_a_device_error_stops_the_bench_without_a_line(capsys):
+    """A kernel that reports a wait that gave up (error word != 0) makes the
+    bench exit non-zero and print no JSON line; a clean word lets it go on."""
+    import pytest
+    import bench
+    bench.require_no_device_error(lambda: 0, "timed device-resident steps")
+    with pytest.raises(SystemExit) as e:
+        bench.require_no_device_error(lambda: 1, "timed device-resident steps")
+    assert e.value.code != 0
+    out = capsys.readouterr()
+    assert out.out == "" and "0x1" in out.err
+
+
+def test_every_timed_region_is_checked_before_the_line_is_printed():
+    """In the native arm, the error word is read after the warm-up, the timed
+    device-resident steps and the timed end-to-end steps, and all of that
+    before the result line is printed."""
+    import ast
+    import inspect
+    import bench
+    tree = ast.parse(inspect.getsource(bench.run_gpu))
+    checks, prints = [], []
+    for node in ast.walk(tree):
+        if isinstance(node, ast.Call) and isinstance(node.func, ast.Name):
+            if node.func.id == "require_no_device_error":
+                checks.append((node.lineno, node.args[1].value))
+            if node.func.id == "print":
+                prints.append(node.lineno)
+    regions = {r for _, r in checks}
+    assert {"warm-up steps", "timed device-resident steps", "timed end-to-end steps"} <= regions
+    assert prints and max(l for l, _ in checks) < min(prints)
