@@ -179,8 +179,25 @@ struct TmaStage {
     static constexpr int kFit = ASR_TMA_SMEM_KB * 1024 / kBytes;
     static constexpr int kStages = kFit < ASR_TMA_STAGES ? kFit : ASR_TMA_STAGES;
     static_assert(kStages >= 2, "need at least two stages");
-    static constexpr int kSmem = kStages * kBytes + 2 * kStages * 8 + TmaShape<PT, GT>::kWarps * 4;
+    static_assert(kBytes % 16 == 0, "stage size keeps 16-byte alignment");
+    // after the stages: full[] and empty[] barriers and the tile index of each
+    // stage (8 B each), the schedule barrier (8 B), the 16-byte schedule
+    // answer (16-byte aligned), one dependency word per consumer warp
+    static constexpr int kBarOff = kStages * kBytes;
+    static constexpr int kTileSlotOff = kBarOff + 16 * kStages;
+    static constexpr int kClcBarOff = kTileSlotOff + 8 * kStages;
+    static constexpr int kClcBufOff = (kClcBarOff + 8 + 15) / 16 * 16;
+    static constexpr int kDepOff = kClcBufOff + 16;
+    static constexpr int kSmem = kDepOff + TmaShape<PT, GT>::kWarps * 4;
 };
+
+// Tile schedule of the pipelined kernel: dynamic (cluster launch control, a
+// grid of one CTA per tile) unless built with ASR_TMA_DYNAMIC=0 (a persistent
+// grid walking the tiles with a fixed stride).
+#ifndef ASR_TMA_DYNAMIC
+#define ASR_TMA_DYNAMIC 1
+#endif
+constexpr uint64_t kNoTile = ~0ull;
 
 // Locate tile `tile` (of tile_elems elements) of a descriptor table, advancing
 // the cursor t.  Tab is AdamTable<CAP> (descriptors in the launch parameters)
@@ -189,6 +206,7 @@ template <typename Tab>
 __device__ __forceinline__ void find_tile(const Tab &tab, uint64_t tile, uint32_t tile_elems, int &t,
                                           uint64_t &off, uint32_t &cnt)
 {
+    if (t > 0 && tile < tab.t[t - 1].tile_end) t = 0;     // tiles normally come in rising order
     while (tile >= tab.t[t].tile_end) ++t;
     const uint64_t first = t == 0 ? 0 : tab.t[t - 1].tile_end;
     off = (tile - first) * static_cast<uint64_t>(tile_elems);
@@ -199,6 +217,11 @@ __device__ __forceinline__ void find_tile(const Tab &tab, uint64_t tile, uint32_
 // The body of the pipelined step, shared by the kernels that differ only in
 // where their descriptor table lives.  All tensors FAST (16-byte-aligned
 // buffers, base % 4 == 0); tile and block shape TmaShape<PT, GT>.
+//
+// The producer decides which tile each stage holds and writes the tile's
+// index into the stage's slot before the stage's barrier completes; the
+// consumers read it after their wait (the barrier orders the two), and a
+// slot holding kNoTile ends their loop.
 template <int PT, int GT, int RM, typename Tab>
 __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, uint64_t limit_ns)
 {
@@ -206,15 +229,17 @@ __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, ui
     using SH = TmaShape<PT, GT>;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t bars = sbase + S::kStages * S::kBytes;      // full[s] then empty[s]
-    auto full = [&](int s) { return bars + 8u * s; };
-    auto empty = [&](int s) { return bars + 8u * (S::kStages + s); };
+    auto full = [&](int s) { return sbase + S::kBarOff + 8u * s; };
+    auto empty = [&](int s) { return sbase + S::kBarOff + 8u * (S::kStages + s); };
+    auto slot = [&](int s) { return sbase + S::kTileSlotOff + 8u * s; };
+    const uint32_t clc_bar = sbase + S::kClcBarOff, clc_buf = sbase + S::kClcBufOff;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::kStages; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), SH::kWarps);
         }
+        mbar_init(clc_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -227,10 +252,25 @@ __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, ui
         asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
         int t = 0;
         uint32_t k = 0;
-        for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+        uint64_t tile = blockIdx.x;           // a CTA's first tile is its own
+#if ASR_TMA_DYNAMIC
+        // one request for the next tile is always in flight, so its answer is
+        // there by the time a stage frees up
+        uint32_t clc_phase = 0;
+        bool asking = true;
+        mbar_arrive_expect_tx(clc_bar, 16);
+        clc_try_cancel(clc_buf, clc_bar);
+#endif
+        for (;; ++k) {
             const int s = static_cast<int>(k % S::kStages);
             const uint32_t use = k / S::kStages;
             if (use > 0 && !mbar_wait(empty(s), (use - 1) & 1u, limit_ns)) break;
+            if (tile >= tab.total_tiles) {
+                st_shared_u64(slot(s), kNoTile);
+                mbar_arrive(full(s));
+                ++k;
+                break;
+            }
             uint64_t off;
             uint32_t cnt;
             find_tile(tab, tile, S::kTile, t, off, cnt);
@@ -238,6 +278,7 @@ __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, ui
             const uint32_t c8 = cnt & ~7u;
             const uint32_t pb = c8 * (PT == ASR_BF16 ? 2u : 4u), gb = c8 * (GT == ASR_BF16 ? 2u : 4u);
             const uint32_t mb = c8 * 4u;
+            st_shared_u64(slot(s), tile);
             mbar_arrive_expect_tx(full(s), pb + gb + 2 * mb);
             if (c8) {
                 const uint32_t dst = sbase + s * S::kBytes;
@@ -248,27 +289,53 @@ __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, ui
                 bulk_load(dst + S::kPBytes + S::kGBytes, T.m + off, mb, full(s), policy);
                 bulk_load(dst + S::kPBytes + S::kGBytes + S::kMBytes, T.v + off, mb, full(s), policy);
             }
+#if ASR_TMA_DYNAMIC
+            // the next tile: the one whose launch the pending request cancelled;
+            // none once a request finds no CTA left (and no request is made
+            // after that)
+            tile = kNoTile;
+            if (asking) {
+                asking = false;
+                if (mbar_wait(clc_bar, clc_phase, limit_ns)) {
+                    clc_phase ^= 1u;
+                    uint32_t x;
+                    if (clc_answer(clc_buf, x)) {
+                        tile = x;
+                        asking = true;
+                        mbar_arrive_expect_tx(clc_bar, 16);
+                        clc_try_cancel(clc_buf, clc_bar);
+                    }
+                }
+            }
+#else
+            tile += gridDim.x;
+#endif
         }
         // Every copy this thread issued must land before the CTA may exit:
-        // wait (bounded) for the last use of each stage.
+        // wait (bounded) for the last use of each stage; likewise for a
+        // schedule request still in flight (only after a failed wait).
         const uint32_t issued = k;
         for (int s = 0; s < S::kStages; ++s) {
             if (static_cast<uint32_t>(s) >= issued) break;
             const uint32_t last_use = (issued - 1 - s) / S::kStages;
             mbar_wait(full(s), last_use & 1u, limit_ns);
         }
+#if ASR_TMA_DYNAMIC
+        if (asking) mbar_wait(clc_bar, clc_phase, limit_ns);
+#endif
         return;
     }
 
     // ---------------------------------------------------------- consumers
     const int ct = threadIdx.x;            // 0 .. SH::kConsumers-1
-    const uint32_t dep_slot = bars + 16u * S::kStages + 4u * warp;   // one word per consumer warp
+    const uint32_t dep_slot = sbase + S::kDepOff + 4u * warp;   // one word per consumer warp
     int t = 0;
-    uint32_t k = 0;
-    for (uint64_t tile = blockIdx.x; tile < tab.total_tiles; tile += gridDim.x, ++k) {
+    for (uint32_t k = 0;; ++k) {
         const int s = static_cast<int>(k % S::kStages);
         const uint32_t use = k / S::kStages;
         if (!mbar_wait(full(s), use & 1u, limit_ns)) return;
+        const uint64_t tile = ld_shared_u64(slot(s));
+        if (tile == kNoTile) return;
         uint64_t off;
         uint32_t cnt;
         find_tile(tab, tile, S::kTile, t, off, cnt);

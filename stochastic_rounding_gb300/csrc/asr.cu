@@ -15,10 +15,13 @@
 // Design (GB300): the optimizer step is a streaming pass, 22 bytes per
 // element for bf16 params/grads with f32 moments, far below the ALU ridge, so
 // its kernels are built for HBM bandwidth.  The hot path (adamw_kernels.cuh)
-// is a persistent kernel, one CTA per SM, in which a producer warp streams
+// is a kernel with one resident CTA per SM, in which a producer warp streams
 // tiles into a shared-memory ring with bulk copies (pipeline.cuh) while
-// consumer warps compute and store; the tensor table of a whole model travels
-// by value (__grid_constant__), so one launch covers it.  Philox runs in
+// consumer warps compute and store; the grid holds one CTA per tile and the
+// running CTAs take the tiles of those not yet started (cluster launch
+// control), so every SM keeps working until the last tile.  The tensor table
+// of a whole model travels by value (__grid_constant__), so one launch covers
+// it.  Philox runs in
 // registers, one 10-round call per four elements, round keys precomputed on
 // the host (common.cuh).  Every float operation is an explicitly rounded IEEE
 // binary32 intrinsic in a fixed order, so results are bit-reproducible.  The
@@ -197,6 +200,20 @@ asr_status tma_grid(K kernel, int threads, int smem, int *grid)
     return ASR_OK;
 }
 
+// Grid of the pipelined kernel for `tiles` tiles.  Dynamic schedule: one CTA
+// per tile (running CTAs take the tiles of CTAs that have not started); fixed
+// schedule: the persistent grid, at most one CTA per tile.
+asr_status tma_launch_grid(uint64_t tiles, int *grid)
+{
+#if ASR_TMA_DYNAMIC
+    if (tiles > 0x7FFFFFFFull) return ASR_ERR_INVALID_VALUE;     // beyond the grid's x limit
+    *grid = static_cast<int>(tiles);
+#else
+    if (static_cast<uint64_t>(*grid) > tiles) *grid = static_cast<int>(tiles);
+#endif
+    return ASR_OK;
+}
+
 template <int PT, int GT, int RM, bool FAST, int CAP>
 asr_status launch_group(const asr_tensor_desc *const *descs, int count, const AdamParams &P, cudaStream_t stream)
 {
@@ -228,7 +245,8 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
         const int smem = TmaStage<PT, GT>::kSmem;
         st = tma_grid(kernel, TmaShape<PT, GT>::kThreads, smem, &grid);
         if (st != ASR_OK) return st;
-        if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
+        st = tma_launch_grid(tiles, &grid);
+        if (st != ASR_OK) return st;
         kernel<<<grid, TmaShape<PT, GT>::kThreads, smem, stream>>>(tab, P, kWaitLimitNs);
     } else {
         auto kernel = adamw_sr_kernel<PT, GT, RM, FAST, CAP>;

@@ -138,6 +138,57 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns)
     mbar_wait(b, 0, limit_ns);
 }
 
+// ------------------------------------------------- dynamic tile schedule
+//
+// Cluster launch control (sm_100 and later): the grid holds one CTA per tile,
+// and a running CTA asks the hardware to cancel the launch of a CTA that has
+// not started yet and takes that CTA's tile instead.  Each SM thus takes a
+// new tile whenever it has room for one, so SMs that the memory system serves
+// faster take more tiles, and every SM finishes within a few tiles of the
+// others.  No global state is involved, and a tile is processed exactly once
+// either way: by its own CTA if that one launches, or by the CTA that
+// cancelled it.
+
+// Asks for one not-yet-started CTA; the 16-byte answer lands at `buf` and
+// completes 16 bytes of transaction count on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t buf, uint32_t bar)
+{
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+                 ::"r"(buf), "r"(bar)
+                 : "memory");
+}
+
+// Reads an answer: true, and the cancelled CTA's x index, if a launch was
+// cancelled; false once no CTA is left to cancel.
+__device__ __forceinline__ bool clc_answer(uint32_t buf, uint32_t &x)
+{
+    uint32_t ok, cx = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
+        "}"
+        : "=r"(ok), "+r"(cx)
+        : "r"(buf)
+        : "memory");
+    x = cx;
+    return ok != 0;
+}
+
+__device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v)
+{
+    asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr)
+{
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
                                           uint64_t policy)
 {

@@ -93,7 +93,8 @@ asr_status launch_static_group(int dev, const TensorEntry *dev_table, uint64_t t
     int grid = 0;
     asr_status st = static_grid(kernel, dev, variant_slot(PT, GT, RM), TmaShape<PT, GT>::kThreads, smem, &grid);
     if (st != ASR_OK) return st;
-    if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
+    st = tma_launch_grid(tiles, &grid);
+    if (st != ASR_OK) return st;
     GlobalTable tab;
     tab.t = dev_table;
     tab.total_tiles = tiles;
