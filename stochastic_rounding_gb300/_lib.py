@@ -130,9 +130,11 @@ def _check(status: int, what: str):
         raise AsrError(status, what)
 
 
+_ROUNDING = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE, ASR_ROUND_SR: ASR_ROUND_SR, ASR_ROUND_RNE: ASR_ROUND_RNE}
+
+
 def make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding="sr") -> AdamwHparams:
-    r = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE, ASR_ROUND_SR: ASR_ROUND_SR,
-         ASR_ROUND_RNE: ASR_ROUND_RNE}.get(rounding)
+    r = _ROUNDING.get(rounding)
     if r is None:
         raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")
     return AdamwHparams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
@@ -150,7 +152,7 @@ def _dev_ptr(t, name, dtypes, numel=None):
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
@@ -161,20 +163,30 @@ def _dev_ptr(t, name, dtypes, numel=None):
     return t.data_ptr()
 
 
+_NULL_CONTEXT = contextlib.nullcontext()
+
+
 def _on_device(device):
     """Make ``device`` current for the call: a no-op (no device switch and
     back) when it already is, which is the common case."""
     torch = _torch()
-    device = torch.device(device)
-    cur = torch.cuda.current_device()
-    if device.index is None or device.index == cur:
-        return contextlib.nullcontext()
+    if not isinstance(device, torch.device):
+        device = torch.device(device)
+    if device.index is None or device.index == torch.cuda.current_device():
+        return _NULL_CONTEXT
     return torch.cuda.device(device)
 
 
 def _stream_handle(device, stream):
+    """The cudaStream_t of ``stream``, or of the device's current stream."""
     torch = _torch()
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            if not isinstance(device, torch.device):
+                device = torch.device(device)
+            idx = device.index if device.index is not None else torch.cuda.current_device()
+            return ctypes.c_void_p(raw(idx))
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
