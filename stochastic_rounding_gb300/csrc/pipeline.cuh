@@ -21,27 +21,43 @@
 #define ASR_TMA_STAGES 4
 #endif
 #ifndef ASR_TMA_SMEM_KB
-#define ASR_TMA_SMEM_KB 200
+#define ASR_TMA_SMEM_KB 224
 #endif
 #ifndef ASR_TMA_EVICT_FIRST
 #define ASR_TMA_EVICT_FIRST 1
 #endif
 
 // Pipeline shape per (param, grad) dtype: the number of consumer warps, one
-// 8-element unit per consumer thread per tile.  Measured on GB300, one
-// 268M-element tensor per combination, all shapes in the same run (GB/s):
-//   bf16/bf16: 20 warps 6,538 (16: 6,232; 12: 5,204) -- the most arithmetic
-//              per byte (Philox and rounding), so the most warps;
-//   bf16/f32:  16 warps 6,669 (20: 6,601; 12: 5,613);
-//   f32/bf16:  12 warps 6,341 (20: 6,079; 16: 6,072);
-//   f32/f32:   12 warps 6,667 (20: 6,071; 16: 6,065) -- with 48 KB tiles
-//              four stages fit where 80 KB tiles allowed two.
+// 8-element unit per consumer thread per tile, and as many stages (at most
+// four) as fit in a 224 KB shared-memory budget.  Measured on GB300 with the
+// dynamic tile schedule, all shapes in the same run, two repetitions (GB/s;
+// bf16/bf16 on the Llama-3-8B set, the others on one 268M-element tensor):
+//   bf16/bf16: 24 warps, 3 stages of 72 KB: 7,078-7,088 (20 warps, 3 stages
+//              in 200 KB: 6,866-6,905; 24 warps, 2 stages: 7,031-7,034;
+//              16 warps: 6,443) -- the most arithmetic per byte (Philox and
+//              rounding), so the most warps;
+//   bf16/f32:  20 warps, 3 stages: 7,073-7,080 (16: 6,533-6,626; 24: 7,033-7,042);
+//   f32/bf16:  16 warps, 4 stages: 7,021-7,031 (12: 6,962-6,968);
+//   f32/f32:   12 warps, 4 stages: 7,066-7,075 (16: 7,022).
+#ifndef ASR_TMA_WARPS_BB
+#define ASR_TMA_WARPS_BB 24             // bf16 params, bf16 grads
+#endif
+#ifndef ASR_TMA_WARPS_BF
+#define ASR_TMA_WARPS_BF 20             // bf16 params, f32 grads
+#endif
+#ifndef ASR_TMA_WARPS_FB
+#define ASR_TMA_WARPS_FB 16             // f32 params, bf16 grads
+#endif
+#ifndef ASR_TMA_WARPS_FF
+#define ASR_TMA_WARPS_FF 12             // f32 params, f32 grads
+#endif
 template <int PT, int GT>
 struct TmaShape {
 #ifdef ASR_TMA_WARPS
     static constexpr int kWarps = ASR_TMA_WARPS;            // one shape for all, for sweeps
 #else
-    static constexpr int kWarps = PT == ASR_BF16 ? (GT == ASR_BF16 ? 20 : 16) : 12;
+    static constexpr int kWarps = PT == ASR_BF16 ? (GT == ASR_BF16 ? ASR_TMA_WARPS_BB : ASR_TMA_WARPS_BF)
+                                                 : (GT == ASR_BF16 ? ASR_TMA_WARPS_FB : ASR_TMA_WARPS_FF);
 #endif
     static constexpr int kConsumers = kWarps * 32;
     static constexpr int kThreads = kConsumers + 32;        // + one producer warp

@@ -99,19 +99,27 @@ def test_unaligned_buffers(asr, orc, off):
     torch.cuda.synchronize()
 
 
-def test_small_and_boundary_sizes(asr, orc):
+# Edges of the pipelined kernel's tiles: 256 elements per consumer warp, 12
+# to 24 warps by dtype combination, so every multiple of 1,024 from 3,072 to
+# 6,144 elements is some combination's tile; one and two tiles, +-1.
+TILE_EDGES = sorted({t * k + d for t in (3072, 4096, 5120, 6144) for k in (1, 2) for d in (-1, 0, 1)})
+
+
+@pytest.mark.parametrize("pdt,gdt", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f32")])
+def test_small_and_boundary_sizes(asr, orc, pdt, gdt):
     import torch
     rng = np.random.default_rng(11)
-    for n in list(range(0, 34)) + [4095, 4096, 4097, 8191, 8193]:
+    sizes = list(range(0, 34)) if pdt == gdt == "bf16" else list(range(0, 34, 7))
+    for n in sizes + TILE_EDGES:
         for base in (0, 1, 3):
-            h = _make(rng, n, "bf16", "bf16")
+            h = _make(rng, n, pdt, gdt)
             # guard bands after the buffers
             full = [dev(np.concatenate([a, np.full(9, 0x7E, a.dtype)])) for a in h]
             d = [t[:n] for t in full]
             _step_both(asr, orc, h, d, step=2, seed=5, base_index=base, **HP)
-            _check(h, d, f"n={n} base={base}")
+            _check(h, d, f"{pdt}/{gdt} n={n} base={base}")
             for t, a in zip(full, h):
-                assert np.all(host(t)[n:] == 0x7E), f"n={n}: wrote past the end"
+                assert np.all(host(t)[n:] == 0x7E), f"{pdt}/{gdt} n={n}: wrote past the end"
     torch.cuda.synchronize()
 
 
