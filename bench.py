@@ -306,27 +306,31 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
     gen = torch.Generator(device=dev)
     gen.manual_seed(1)
 
-    def timed(fn):
+    def timed(fn, reps=steps):
         for t in range(1, warmup + 1):
             fn(t)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for t in range(warmup + 1, warmup + steps + 1):
+        for t in range(warmup + 1, warmup + reps + 1):
             fn(t)
         e1.record()
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) / steps
+        return e0.elapsed_time(e1) / reps
 
     def single(name, n, pdt, gdt, bpp, note):
         p = W.device_normal_(torch.empty(n, dtype=pdt, device=dev), gen, 0.02)
         g = W.device_normal_(torch.empty(n, dtype=gdt, device=dev), gen, 1e-3)
         m = torch.zeros(n, device=dev)
         v = torch.zeros(n, device=dev)
-        ms = timed(lambda t: asr.asr_adamw_sr_step(p, g, m, v, step=t, seed=0, **HP))
+        # steps of a millisecond or less: at least 50 timed launches, so the
+        # host's gap before the first one (the GPU idles while the call is
+        # prepared) is spread thin
+        reps = max(steps, 50)
+        ms = timed(lambda t: asr.asr_adamw_sr_step(p, g, m, v, step=t, seed=0, **HP), reps)
         gbs = bpp * n / ms / 1e6
         out[name] = {"params": n, "ms_per_step": ms, "gparams_per_s": n / ms / 1e6, "bytes_per_param": bpp,
-                     "gbs": gbs, "frac_of_measured_copy": gbs / peak, "note": note}
+                     "gbs": gbs, "frac_of_measured_copy": gbs / peak, "timed_steps": reps, "note": note}
         del p, g, m, v
 
     single("single_65536_bf16", 65536, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM,
@@ -350,6 +354,42 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
     out["sr_op_1073741824"] = elementwise_measure(asr, dev, "sr", 1 << 30, steps, warmup)
     out["philox_268435456"] = elementwise_measure(asr, dev, "philox", 1 << 28, steps, warmup)
     torch.cuda.empty_cache()
+    return out
+
+
+def optimizer_step_time(asr, tensors, dev, steps, warmup, n):
+    """The user-facing optimizer (AdamWSR.step()) on the same 8B set: wall
+    time per step over `steps` steps after `warmup`, with the blocking and
+    with the deferred device-error check.  Its moments are the set's own
+    buffers (placed in the optimizer state as a loaded checkpoint would be),
+    so no memory is added."""
+    import torch
+    params = []
+    for p, g, m, v, base in tensors:
+        prm = torch.nn.Parameter(p)
+        prm.grad = g
+        params.append(prm)
+    out = {}
+    for mode in (True, "deferred"):
+        opt = asr.AdamWSR(params, lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                          weight_decay=HP["weight_decay"], seed=0, check_errors=mode)
+        for prm, (p, g, m, v, base) in zip(params, tensors):
+            opt.state[prm] = {"step": 0, "exp_avg": m, "exp_avg_sq": v}
+        for _ in range(warmup):
+            opt.step()
+        opt.poll_errors(wait=True)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            opt.step()
+        opt.poll_errors(wait=True)
+        torch.cuda.synchronize(dev)
+        ms = (time.perf_counter() - t0) / steps * 1e3
+        out["blocking_check" if mode is True else "deferred_check"] = {
+            "ms_per_step": ms, "gparams_per_s": n / ms / 1e6}
+        del opt
+    out["note"] = ("AdamWSR.step() on the 8B set (291 parameters), wall clock with a synchronize at the end; "
+                   "the blocking check waits for each step, the deferred one reads the error word one step late")
     return out
 
 
@@ -572,7 +612,8 @@ def run_gpu(args):
 
     others = None
     if rank == 0 and not args.params:
-        others = measure_configs(asr, W, dev, args.steps, args.warmup, peak)
+        others = {"optimizer_class_8b": optimizer_step_time(asr, tensors, dev, args.steps, args.warmup, n)}
+        others.update(measure_configs(asr, W, dev, args.steps, args.warmup, peak))
 
     cpu = None
     if rank == 0:

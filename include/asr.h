@@ -229,11 +229,23 @@ const char *asr_status_string(asr_status status);
 int asr_last_cuda_error(void);
 
 /* Sticky error bits raised on the device by the current device's kernels,
- * read and cleared.  Bit 0 (1): a pipeline wait inside a kernel gave up
- * after its time limit (2 s); the kernel then left the affected tiles
- * unfinished and returned instead of hanging.  Waits for `stream`, then
- * stores the bits (0 = no error) in *bits (host). */
+ * read and cleared in one atomic step.  Bit 0 (1): a pipeline wait inside a
+ * kernel gave up after its time limit (2 s); the kernel then left the
+ * affected tiles unfinished and returned instead of hanging.  Enqueues the
+ * read on `stream`, waits for the stream, then stores the bits (0 = no
+ * error) in *bits (host). */
 asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream);
+
+/* The same as asr_take_device_error without waiting (no counterpart on the
+ * pages): enqueues on `stream` one thread that atomically reads and clears
+ * the current device's error bits and writes them to *bits, and returns.
+ * *bits holds the value once the stream has reached that point (wait for an
+ * event recorded after the call).  bits: 4-byte aligned memory the GPU can
+ * write -- device or managed memory of the current device, or page-locked
+ * host memory (cudaHostAlloc / cudaMallocHost / cudaHostRegister); any other
+ * pointer (pageable host memory, NULL) returns ASR_ERR_INVALID_VALUE and
+ * launches nothing. */
+asr_status asr_take_device_error_async(uint32_t *bits, asr_stream_t stream);
 
 /* Diagnostic (no counterpart on the pages): launches one thread that waits,
  * with the kernels' bounded-wait routine and a limit of limit_ns

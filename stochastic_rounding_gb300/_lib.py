@@ -24,7 +24,7 @@ ASR_ROUND_SR, ASR_ROUND_RNE = 0, 1
 EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
            "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
            "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout",
-           "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr")
+           "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr", "asr_take_device_error_async")
 ASR_STATIC_TABLE_MAX = 4096
 
 
@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
         L.asr_selftest_wait_timeout.restype = ctypes.c_int
         L.asr_take_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.asr_take_device_error.restype = ctypes.c_int
+        L.asr_take_device_error_async.argtypes = [vp, vp]
+        L.asr_take_device_error_async.restype = ctypes.c_int
         L.asr_last_cuda_error.argtypes = []
         L.asr_last_cuda_error.restype = ctypes.c_int
         _lib = L
@@ -114,6 +116,25 @@ def asr_take_device_error(stream=None, device=None) -> int:
         _check(lib().asr_take_device_error(ctypes.byref(bits), _stream_handle(dev, stream)),
                "asr_take_device_error")
     return int(bits.value)
+
+
+def asr_take_device_error_async(out, stream=None, device=None):
+    """Enqueue a read-and-clear of the device error bits into ``out`` (a
+    one-element int32 tensor: page-locked CPU memory, or on the CUDA device)
+    without waiting; ``out`` holds the bits once the stream gets there."""
+    torch = _torch()
+    if not isinstance(out, torch.Tensor) or out.dtype != torch.int32 or out.numel() != 1:
+        raise TypeError("out must be a one-element int32 tensor")
+    if out.is_cuda:
+        dev = out.device
+    else:
+        if not out.is_pinned():
+            raise ValueError("out must be page-locked (pin_memory=True) or a CUDA tensor")
+        dev = torch.device(device if device is not None else "cuda")
+    with _on_device(dev):
+        _check(lib().asr_take_device_error_async(ctypes.c_void_p(out.data_ptr()), _stream_handle(dev, stream)),
+               "asr_take_device_error_async")
+    return out
 
 
 def asr_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None, device=None):

@@ -49,6 +49,18 @@ namespace {
 #include "adamw_kernels.cuh"
 #include "rounding_kernels.cuh"
 
+// Takes the device error bits: reads and clears the word in one atomic step
+// (so no bit set by a kernel still running elsewhere is lost between the two)
+// and writes them to dst -- device memory, or page-locked host memory that
+// the GPU can write -- or, with dst null, to g_error_taken.
+__device__ unsigned int g_error_taken = 0;
+
+__global__ void take_error_kernel(unsigned int *dst)
+{
+    const unsigned int bits = atomicExch(&g_device_error, 0u);
+    *(dst ? dst : &g_error_taken) = bits;
+}
+
 // ------------------------------------------------------------- host side
 
 thread_local int g_last_cuda_error = 0;
@@ -370,13 +382,34 @@ asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream)
 {
     if (!bits) return ASR_ERR_INVALID_VALUE;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    unsigned int h = 0, zero = 0;
-    cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_device_error, sizeof(h), 0, cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    take_error_kernel<<<1, 1, 0, s>>>(nullptr);
+    cudaError_t e = cudaGetLastError();
+    unsigned int h = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&h, g_error_taken, sizeof(h), 0, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e);
     *bits = h;
     return ASR_OK;
+}
+
+asr_status asr_take_device_error_async(uint32_t *bits, asr_stream_t stream)
+{
+    if (!bits || (reinterpret_cast<uintptr_t>(bits) & 3u)) return ASR_ERR_INVALID_VALUE;
+    // Only memory the GPU can write: device or managed memory, or page-locked
+    // host memory (written through its device-side address).
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, bits);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged && a.type != cudaMemoryTypeHost)
+        return ASR_ERR_INVALID_VALUE;
+    if (!a.devicePointer) return ASR_ERR_INVALID_VALUE;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (a.type == cudaMemoryTypeDevice && a.device != dev) return ASR_ERR_INVALID_VALUE;
+    take_error_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned int *>(a.devicePointer));
+    return check_launch();
 }
 
 asr_status asr_adamw_prepare(const asr_adamw_hparams *hp, asr_adamw_scalars *out)

@@ -21,16 +21,20 @@ across shards and ranks).  Every step of a group is one multi-tensor launch
 
 Device errors: the kernels' pipeline waits give up after a time limit rather
 than hang, leaving the step incomplete and raising a sticky device error bit.
-With ``check_errors`` (the default) every ``step()`` reads that bit once its
-launches are queued, which waits for the step to finish on the device (one
-host synchronisation per step), and raises ``DeviceError`` if it is set.
-``check_errors=False`` skips the read (no synchronisation); the caller then
-checks with ``stochastic_rounding_gb300.asr_take_device_error`` when it
-wants to.
+``check_errors`` says when ``step()`` looks at it:
+  - ``True`` (the default): once the step's launches are queued it reads the
+    bit, which waits for the step to finish on the device (one host
+    synchronisation per step), and raises ``DeviceError`` if it is set;
+  - ``"deferred"``: it queues the read behind the step into page-locked host
+    memory without waiting, and raises ``DeviceError`` at a later ``step()``
+    (or ``poll_errors()``) once that read has landed -- the host keeps
+    running ahead of the GPU, and an error is reported a step or two late;
+  - ``False``: no read; the caller checks with
+    ``stochastic_rounding_gb300.asr_take_device_error`` when it wants to.
 """
 from __future__ import annotations
 
-from typing import Dict, List, Optional
+from typing import Dict, List
 
 import torch
 
@@ -50,14 +54,14 @@ class AdamWSR(torch.optim.Optimizer):
     ``weight_decay``) plus ``seed`` (64-bit key of the rounding stream) and
     ``rounding`` (``"sr"``, or ``"rne"`` for round-to-nearest-even, the
     biased baseline), ``base_offset`` (global position of the first
-    parameter's element 0) and ``check_errors`` (read the device error bit
-    after every step).  Parameters must be contiguous CUDA tensors of float32
+    parameter's element 0) and ``check_errors`` (when to read the device
+    error bit: ``True``, ``"deferred"`` or ``False``, see the module notes).  Parameters must be contiguous CUDA tensors of float32
     or bfloat16; gradients dense float32 or bfloat16.
     """
 
     def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
                  weight_decay: float = 1e-2, *, seed: int = 0, rounding: str = "sr",
-                 base_offset: int = 0, check_errors: bool = True):
+                 base_offset: int = 0, check_errors=True):
         if not 0.0 <= lr:
             raise ValueError(f"Invalid learning rate: {lr}")
         if not 0.0 <= eps:
@@ -75,7 +79,8 @@ class AdamWSR(torch.optim.Optimizer):
         if not 0 <= int(base_offset) < 2**64:
             raise ValueError("base_offset must fit in 64 bits")
         self.base_offset = int(base_offset)
-        self.check_errors = bool(check_errors)
+        self.check_errors = self._error_mode(check_errors)
+        self._pending: Dict[torch.device, List[tuple]] = {}
         defaults = dict(lr=lr, betas=tuple(betas), eps=eps, weight_decay=weight_decay,
                         seed=int(seed), rounding=rounding, base_index=None)
         super().__init__(params, defaults)
@@ -103,6 +108,43 @@ class AdamWSR(torch.optim.Optimizer):
         if hasattr(self, "_base"):
             self._assign_positions()
 
+    @staticmethod
+    def _error_mode(mode):
+        if mode is True or mode is False or mode == "deferred":
+            return mode
+        raise ValueError(f"check_errors must be True, False or 'deferred', not {mode!r}")
+
+    # Reads of the error word queued by "deferred" steps: per device a list of
+    # (event, page-locked one-word tensor), oldest first, at most this many.
+    _MAX_PENDING = 4
+
+    def poll_errors(self, wait: bool = False):
+        """Look at the error reads queued by earlier "deferred" steps: those
+        already landed (all of them, waiting, with ``wait``).  Raises
+        ``DeviceError`` if any found a bit set."""
+        bad = []
+        for device, queue in self._pending.items():
+            while queue and (wait or queue[0][0].query()):
+                event, word = queue.pop(0)
+                event.synchronize()
+                if int(word.item()):
+                    bad.append((device, int(word.item())))
+        if bad:
+            device, bits = bad[0]
+            raise DeviceError(f"AdamWSR: device error bits {bits:#x} on {device} from an earlier step "
+                              "(a pipeline wait gave up; that step is incomplete)")
+
+    def _queue_error_read(self, device):
+        queue = self._pending.setdefault(device, [])
+        if len(queue) >= self._MAX_PENDING:
+            queue[0][0].synchronize()
+            self.poll_errors()
+        word = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+        _lib.asr_take_device_error_async(word, device=device)
+        event = torch.cuda.Event()
+        event.record(torch.cuda.current_stream(device))
+        queue.append((event, word))
+
     def base_index(self, p: torch.Tensor) -> int:
         """Global parameter position of element 0 of ``p``."""
         return self._base[id(p)]
@@ -124,9 +166,12 @@ class AdamWSR(torch.optim.Optimizer):
             raise ValueError("gradient must be contiguous, on the parameter's device and of its shape")
 
     @torch.no_grad()
-    def step(self, closure=None, *, check_errors: Optional[bool] = None):
+    def step(self, closure=None, *, check_errors=None):
         """One AdamW-SR step of every parameter that has a gradient.
         ``check_errors`` overrides the optimizer's setting for this call."""
+        mode = self.check_errors if check_errors is None else self._error_mode(check_errors)
+        if self._pending:
+            self.poll_errors()
         loss = None
         if closure is not None:
             with torch.enable_grad():
@@ -158,7 +203,10 @@ class AdamWSR(torch.optim.Optimizer):
                     weight_decay=group["weight_decay"], step=step, seed=group["seed"],
                     rounding=group["rounding"], device=device)
                 devices.add(device)
-        if self.check_errors if check_errors is None else check_errors:
+        if mode == "deferred":
+            for device in devices:
+                self._queue_error_read(device)
+        elif mode:
             for device in devices:
                 bits = _lib.asr_take_device_error(device=device)
                 if bits:

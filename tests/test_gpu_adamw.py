@@ -302,6 +302,39 @@ def test_bounded_wait_gives_up_with_a_status(asr):
     assert asr.asr_take_device_error() == 0
 
 
+def test_error_bits_taken_without_waiting(asr):
+    """asr_take_device_error_async: after a wait that gave up (the self-test)
+    the bits land in page-locked host memory, or in device memory, once the
+    stream gets there, and the word is clear afterwards.  Memory the GPU
+    cannot write (pageable host memory, NULL, misaligned) is refused before
+    anything is launched."""
+    import ctypes
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    asr.asr_take_device_error()
+    for target in ("pinned", "cuda"):
+        word = (torch.full((1,), -1, dtype=torch.int32, pin_memory=True) if target == "pinned"
+                else torch.full((1,), -1, dtype=torch.int32, device="cuda"))
+        asr.asr_selftest_wait_timeout(1_000_000)
+        asr.asr_take_device_error_async(word)
+        torch.cuda.synchronize()
+        assert int(word.item()) == 1, target
+        asr.asr_take_device_error_async(word)
+        torch.cuda.synchronize()
+        assert int(word.item()) == 0, target
+    assert asr.asr_take_device_error() == 0
+    L = _lib.lib()
+    pageable = np.zeros(4, np.uint32)
+    sh = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.asr_take_device_error_async(ctypes.c_void_p(pageable.ctypes.data), sh) == _lib.ASR_ERR_INVALID_VALUE
+    assert L.asr_take_device_error_async(None, sh) == _lib.ASR_ERR_INVALID_VALUE
+    pinned = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+    assert L.asr_take_device_error_async(ctypes.c_void_p(pinned.data_ptr() + 2), sh) == _lib.ASR_ERR_INVALID_VALUE
+    with pytest.raises(ValueError):
+        asr.asr_take_device_error_async(torch.zeros(1, dtype=torch.int32))
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("pdt,gdt,n,steps", [("bf16", "bf16", 48_000_000 + 4096 * 3 + 8, 24),
                                              ("f32", "f32", 16_777_216, 40),
                                              ("bf16", "f32", 20_000_000, 16)])

@@ -333,3 +333,32 @@ def test_step_raises_after_a_device_error(asr):
     asr.asr_selftest_wait_timeout(1_000_000)
     opt.step(check_errors=False)               # not read here ...
     assert asr.asr_take_device_error() == 1    # ... so it is still set
+
+
+def test_deferred_error_check(asr):
+    """check_errors="deferred": steps do not wait for the GPU; a device error
+    raised during one step is reported by a later step() or by
+    poll_errors(wait=True), and clean steps report nothing.  The parameters
+    end as with the blocking check."""
+    import torch
+    a = _params(torch.bfloat16, 8)
+    b = [torch.nn.Parameter(p.detach().clone()) for p in a]
+    oa = asr.AdamWSR(a, **HP, seed=3, check_errors="deferred")
+    ob = asr.AdamWSR(b, **HP, seed=3)
+    asr.asr_take_device_error()
+    for step in range(1, 7):
+        for p, q, g in zip(a, b, _grads(a, step)):
+            p.grad = g
+            q.grad = g.clone()
+        oa.step()
+        ob.step()
+    oa.poll_errors(wait=True)
+    for p, q in zip(a, b):
+        assert torch.equal(_bits(p), _bits(q))
+    asr.asr_selftest_wait_timeout(1_000_000)
+    oa.step()                                   # the bit is taken behind this step
+    with pytest.raises(asr.DeviceError):
+        oa.poll_errors(wait=True)
+    oa.step()
+    oa.poll_errors(wait=True)                   # clean again
+    assert asr.asr_take_device_error() == 0

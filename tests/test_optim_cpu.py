@@ -7,7 +7,7 @@ from stochastic_rounding_gb300.optim import AdamWSR
 
 @pytest.mark.parametrize("kw", [dict(lr=-1.0), dict(eps=-1e-8), dict(betas=(1.0, 0.999)),
                                 dict(betas=(0.9, -0.1)), dict(weight_decay=-0.1), dict(rounding="up"),
-                                dict(seed=2**64)])
+                                dict(seed=2**64), dict(check_errors="later"), dict(check_errors=2)])
 def test_rejects_bad_arguments(kw):
     p = torch.nn.Parameter(torch.zeros(4))
     with pytest.raises(ValueError):
