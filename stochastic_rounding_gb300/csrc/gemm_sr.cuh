@@ -494,9 +494,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     return pair_wait_slow<true>(bar, parity, limit_ns);
 }
 
+// Arrival of an epilogue warp on the first CTA's accumulator-empty barrier.
+// Relaxed: the MMA warp waiting there reuses only the tensor memory, whose
+// reads (tcgen05.ld) have completed at the epilogue's tcgen05.wait::ld, so
+// nothing has to be released -- a release arrive at cluster scope would
+// make the warp wait for its own global stores of the tile to be visible
+// (measured as the "membar" stall, 1.3 per issued instruction at K = 512).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
