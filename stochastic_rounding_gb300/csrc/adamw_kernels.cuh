@@ -66,7 +66,9 @@ __device__ __forceinline__ float vec_g(const VecUnit<PT, GT> &u, int k)
     return __uint_as_float(u.g[k]);
 }
 
-template <int PT, int GT, int RM>
+// A4: the tensor's base index is a multiple of 4, so the unit's eight random
+// words come from two Philox counters; otherwise from three (unit_words).
+template <int PT, int GT, int RM, bool A4 = true>
 __device__ __forceinline__ void vec_compute_store(const TensorEntry &T, uint64_t e, VecUnit<PT, GT> &u,
                                                   const AdamParams &P)
 {
@@ -78,7 +80,7 @@ __device__ __forceinline__ void vec_compute_store(const TensorEntry &T, uint64_t
         uint32_t w[4];
         if (RM == ASR_ROUND_SR) {
             uint32_t r[8];
-            unit_words<true>(T.base, e, P.step, P.keys, r);
+            unit_words<A4>(T.base, e, P.step, P.keys, r);
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = sr_pack2<ASR_ADAMW_CVT_RS>(pn[2 * k], pn[2 * k + 1], r[2 * k], r[2 * k + 1]);
         } else {
@@ -215,14 +217,16 @@ __device__ __forceinline__ void find_tile(const Tab &tab, uint64_t tile, uint32_
 }
 
 // The body of the pipelined step, shared by the kernels that differ only in
-// where their descriptor table lives.  All tensors FAST (16-byte-aligned
-// buffers, base % 4 == 0); tile and block shape TmaShape<PT, GT>.
+// where their descriptor table lives.  Every tensor has 16-byte-aligned
+// buffers, and with A4 a base index that is a multiple of 4 (without A4 the
+// bases may be anything: each unit then draws three Philox counters instead
+// of two); tile and block shape TmaShape<PT, GT>.
 //
 // The producer decides which tile each stage holds and writes the tile's
 // index into the stage's slot before the stage's barrier completes; the
 // consumers read it after their wait (the barrier orders the two), and a
 // slot holding kNoTile ends their loop.
-template <int PT, int GT, int RM, typename Tab>
+template <int PT, int GT, int RM, bool A4, typename Tab>
 __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, uint64_t limit_ns)
 {
     using S = TmaStage<PT, GT>;
@@ -399,7 +403,7 @@ __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, ui
 #pragma unroll
         for (int j = 0; j < SH::kUnits; ++j) {
             const uint32_t e = (static_cast<uint32_t>(j) * SH::kConsumers + ct) * kVec;
-            if (e < c8) vec_compute_store<PT, GT, RM>(T, off + e, u[j], P);
+            if (e < c8) vec_compute_store<PT, GT, RM, A4>(T, off + e, u[j], P);
         }
         // a ragged end of a tensor (< 8 elements) goes through the scalar path
         if (c8 < cnt && ct == (c8 / kVec) % SH::kConsumers) scalar_unit<PT, GT, RM>(T, off + c8, P);
@@ -407,10 +411,10 @@ __device__ __forceinline__ void tma_step(const Tab &tab, const AdamParams &P, ui
 }
 
 // Descriptor table in the launch parameters (up to CAP tensors).
-template <int PT, int GT, int RM, int CAP>
+template <int PT, int GT, int RM, int CAP, bool A4>
 __global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
 adamw_sr_tma_kernel(const __grid_constant__ AdamTable<CAP> tab, const __grid_constant__ AdamParams P,
                     uint64_t limit_ns)
 {
-    tma_step<PT, GT, RM>(tab, P, limit_ns);
+    tma_step<PT, GT, RM, A4>(tab, P, limit_ns);
 }

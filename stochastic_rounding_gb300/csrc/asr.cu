@@ -171,15 +171,30 @@ asr_status validate_desc(const asr_tensor_desc &d)
     return ASR_OK;
 }
 
-bool desc_fast(const asr_tensor_desc &d)
-{
-    return aligned16(d.param) && aligned16(d.grad) && aligned16(d.exp_avg) && aligned16(d.exp_avg_sq) &&
-           (d.base_index & 3u) == 0;
-}
-
 #ifndef ASR_USE_TMA
 #define ASR_USE_TMA 1
 #endif
+
+// Which kernel updates a tensor.
+//   kPlainPath: buffers not all 16-byte aligned -- the register-resident
+//     kernel with scalar units;
+//   kVecA4: 16-byte-aligned buffers and either a base index that is a
+//     multiple of 4 or no random bits needed (f32 params, nearest rounding)
+//     -- the pipelined kernel, two Philox counters per 8-element unit;
+//   kVecAnyBase: 16-byte-aligned buffers, stochastic rounding of bf16
+//     params, base index not a multiple of 4 -- the pipelined kernel drawing
+//     three counters per unit.  A model whose parameters are numbered end to
+//     end gets such bases after any parameter of odd size.
+constexpr int kPlainPath = 0, kVecA4 = 1, kVecAnyBase = 2;
+
+int desc_class(const asr_tensor_desc &d, int rounding)
+{
+    if (!(aligned16(d.param) && aligned16(d.grad) && aligned16(d.exp_avg) && aligned16(d.exp_avg_sq)))
+        return kPlainPath;
+    const bool bits = d.param_dtype == ASR_BF16 && rounding == ASR_ROUND_SR;
+    if ((d.base_index & 3u) == 0 || !bits) return kVecA4;
+    return ASR_USE_TMA ? kVecAnyBase : kPlainPath;
+}
 
 // Dynamic shared memory opt-in and persistent grid of the bulk-copy kernel,
 // cached per (device, kernel).
@@ -226,11 +241,11 @@ asr_status tma_launch_grid(uint64_t tiles, int *grid)
     return ASR_OK;
 }
 
-template <int PT, int GT, int RM, bool FAST, int CAP>
+template <int PT, int GT, int RM, int CLS, int CAP>
 asr_status launch_group(const asr_tensor_desc *const *descs, int count, const AdamParams &P, cudaStream_t stream)
 {
     static_assert(CAP >= 1, "");
-    constexpr bool kTma = FAST && ASR_USE_TMA;
+    constexpr bool kTma = CLS != kPlainPath && ASR_USE_TMA;
     constexpr uint64_t tile = kTma ? TmaShape<PT, GT>::kTile : kTile;
     AdamTable<CAP> tab;
     std::memset(&tab, 0, sizeof(tab));
@@ -252,8 +267,8 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
     if (tiles == 0) return ASR_OK;
     int grid = 0;
     asr_status st;
-    if (kTma) {
-        auto kernel = adamw_sr_tma_kernel<PT, GT, RM, CAP>;
+    if constexpr (kTma) {
+        auto kernel = adamw_sr_tma_kernel<PT, GT, RM, CAP, CLS == kVecA4>;
         const int smem = TmaStage<PT, GT>::kSmem;
         st = tma_grid(kernel, TmaShape<PT, GT>::kThreads, smem, &grid);
         if (st != ASR_OK) return st;
@@ -261,7 +276,7 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
         if (st != ASR_OK) return st;
         kernel<<<grid, TmaShape<PT, GT>::kThreads, smem, stream>>>(tab, P, kWaitLimitNs);
     } else {
-        auto kernel = adamw_sr_kernel<PT, GT, RM, FAST, CAP>;
+        auto kernel = adamw_sr_kernel<PT, GT, RM, CLS == kVecA4, CAP>;
         st = persistent_grid(kernel, &grid);
         if (st != ASR_OK) return st;
         if (static_cast<uint64_t>(grid) > tiles) grid = static_cast<int>(tiles);
@@ -270,39 +285,42 @@ asr_status launch_group(const asr_tensor_desc *const *descs, int count, const Ad
     return check_launch();
 }
 
-template <int PT, int GT, int RM, bool FAST>
+template <int PT, int GT, int RM, int CLS>
 asr_status launch_chunks(const asr_tensor_desc *const *descs, int count, const AdamParams &P, cudaStream_t stream)
 {
-    if (count == 1) return launch_group<PT, GT, RM, FAST, kCapSmall>(descs, 1, P, stream);
+    if (count == 1) return launch_group<PT, GT, RM, CLS, kCapSmall>(descs, 1, P, stream);
     for (int s = 0; s < count; s += kCapLarge) {
         const int c = count - s < kCapLarge ? count - s : kCapLarge;
-        asr_status st = launch_group<PT, GT, RM, FAST, kCapLarge>(descs + s, c, P, stream);
+        asr_status st = launch_group<PT, GT, RM, CLS, kCapLarge>(descs + s, c, P, stream);
         if (st != ASR_OK) return st;
     }
     return ASR_OK;
 }
 
 template <int PT, int GT, int RM>
-asr_status dispatch_fast(const asr_tensor_desc *const *descs, int count, bool fast, const AdamParams &P,
-                         cudaStream_t stream)
+asr_status dispatch_class(const asr_tensor_desc *const *descs, int count, int cls, const AdamParams &P,
+                          cudaStream_t stream)
 {
-    return fast ? launch_chunks<PT, GT, RM, true>(descs, count, P, stream)
-                : launch_chunks<PT, GT, RM, false>(descs, count, P, stream);
+    if (cls == kPlainPath) return launch_chunks<PT, GT, RM, kPlainPath>(descs, count, P, stream);
+    if constexpr (PT == ASR_BF16 && RM == ASR_ROUND_SR) {
+        if (cls == kVecAnyBase) return launch_chunks<PT, GT, RM, kVecAnyBase>(descs, count, P, stream);
+    }
+    return launch_chunks<PT, GT, RM, kVecA4>(descs, count, P, stream);
 }
 
-asr_status dispatch(const asr_tensor_desc *const *descs, int count, int pdt, int gdt, int rm, bool fast,
+asr_status dispatch(const asr_tensor_desc *const *descs, int count, int pdt, int gdt, int rm, int cls,
                     const AdamParams &P, cudaStream_t stream)
 {
     if (pdt == ASR_BF16) {
         if (gdt == ASR_BF16)
-            return rm == ASR_ROUND_SR ? dispatch_fast<ASR_BF16, ASR_BF16, ASR_ROUND_SR>(descs, count, fast, P, stream)
-                                      : dispatch_fast<ASR_BF16, ASR_BF16, ASR_ROUND_RNE>(descs, count, fast, P, stream);
-        return rm == ASR_ROUND_SR ? dispatch_fast<ASR_BF16, ASR_F32, ASR_ROUND_SR>(descs, count, fast, P, stream)
-                                  : dispatch_fast<ASR_BF16, ASR_F32, ASR_ROUND_RNE>(descs, count, fast, P, stream);
+            return rm == ASR_ROUND_SR ? dispatch_class<ASR_BF16, ASR_BF16, ASR_ROUND_SR>(descs, count, cls, P, stream)
+                                      : dispatch_class<ASR_BF16, ASR_BF16, ASR_ROUND_RNE>(descs, count, cls, P, stream);
+        return rm == ASR_ROUND_SR ? dispatch_class<ASR_BF16, ASR_F32, ASR_ROUND_SR>(descs, count, cls, P, stream)
+                                  : dispatch_class<ASR_BF16, ASR_F32, ASR_ROUND_RNE>(descs, count, cls, P, stream);
     }
     // f32 params are stored as computed: the rounding mode does not apply.
-    if (gdt == ASR_BF16) return dispatch_fast<ASR_F32, ASR_BF16, ASR_ROUND_SR>(descs, count, fast, P, stream);
-    return dispatch_fast<ASR_F32, ASR_F32, ASR_ROUND_SR>(descs, count, fast, P, stream);
+    if (gdt == ASR_BF16) return dispatch_class<ASR_F32, ASR_BF16, ASR_ROUND_SR>(descs, count, cls, P, stream);
+    return dispatch_class<ASR_F32, ASR_F32, ASR_ROUND_SR>(descs, count, cls, P, stream);
 }
 
 asr_status run_adamw(const asr_tensor_desc *table, int32_t n_tensors, const asr_adamw_hparams *hp,
@@ -320,7 +338,7 @@ asr_status run_adamw(const asr_tensor_desc *table, int32_t n_tensors, const asr_
     P.keys = make_keys(hp->seed);
     P.step = hp->step;
 
-    // Group by (param dtype, grad dtype, vector eligibility), keeping order.
+    // Group by (param dtype, grad dtype, kernel class), keeping order.
     // Every element is independent, so the grouping cannot change any bit.
     const int nt = n_tensors;
     const asr_tensor_desc **sel = nullptr;
@@ -332,18 +350,19 @@ asr_status run_adamw(const asr_tensor_desc *table, int32_t n_tensors, const asr_
         holder.reset(new const asr_tensor_desc *[nt]);
         sel = holder.get();
     }
+    const int rm = static_cast<int>(hp->rounding);
     for (int pdt = 0; pdt < 2; ++pdt)
         for (int gdt = 0; gdt < 2; ++gdt)
-            for (int f = 0; f < 2; ++f) {
+            for (int cls = kPlainPath; cls <= kVecAnyBase; ++cls) {
                 int c = 0;
                 for (int i = 0; i < nt; ++i) {
                     const asr_tensor_desc &d = table[i];
-                    if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || desc_fast(d) != (f == 1))
+                    if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || desc_class(d, rm) != cls)
                         continue;
                     sel[c++] = &d;
                 }
                 if (c == 0) continue;
-                st = dispatch(sel, c, pdt, gdt, static_cast<int>(hp->rounding), f == 1, P, stream);
+                st = dispatch(sel, c, pdt, gdt, rm, cls, P, stream);
                 if (st != ASR_OK) return st;
             }
     return ASR_OK;

@@ -23,12 +23,12 @@ struct GlobalTable {
 };
 
 // The pipelined step with its table read from global memory (g_static_table).
-template <int PT, int GT, int RM>
+template <int PT, int GT, int RM, bool A4>
 __global__ void __launch_bounds__(TmaShape<PT, GT>::kThreads, 1)
 adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid_constant__ AdamParams P,
                            uint64_t limit_ns)
 {
-    tma_step<PT, GT, RM>(tab, P, limit_ns);
+    tma_step<PT, GT, RM, A4>(tab, P, limit_ns);
 }
 
 // Per-device set-up of this path, kept in fixed arrays (no allocation): the
@@ -37,7 +37,8 @@ adamw_sr_tma_static_kernel(const __grid_constant__ GlobalTable tab, const __grid
 // cudaGetSymbolAddress while the device is current -- and the persistent grid
 // of each kernel variant.
 constexpr int kMaxDevices = 64;
-constexpr int kStaticVariants = 12;        // 6 dtype/rounding combinations x {pipelined, plain}
+constexpr int kStaticVariants = 18;        // 6 dtype/rounding combinations x {pipelined with bases that are
+                                           // multiples of 4, pipelined with any base, plain}
 std::mutex g_static_mu;
 TensorEntry *g_static_addr[kMaxDevices];
 int g_static_grid[kMaxDevices][kStaticVariants];
@@ -84,14 +85,15 @@ std::mutex g_stage_mu;
 TensorEntry g_stage_table[kStaticTableMax];
 AdamTable<kCapLarge> g_stage_plain;
 
-template <int PT, int GT, int RM>
+template <int PT, int GT, int RM, bool A4>
 asr_status launch_static_group(int dev, const TensorEntry *dev_table, uint64_t tiles, const AdamParams &P,
                                cudaStream_t stream)
 {
-    auto kernel = adamw_sr_tma_static_kernel<PT, GT, RM>;
+    auto kernel = adamw_sr_tma_static_kernel<PT, GT, RM, A4>;
     const int smem = TmaStage<PT, GT>::kSmem;
     int grid = 0;
-    asr_status st = static_grid(kernel, dev, variant_slot(PT, GT, RM), TmaShape<PT, GT>::kThreads, smem, &grid);
+    asr_status st = static_grid(kernel, dev, (A4 ? 0 : 6) + variant_slot(PT, GT, RM), TmaShape<PT, GT>::kThreads,
+                                smem, &grid);
     if (st != ASR_OK) return st;
     st = tma_launch_grid(tiles, &grid);
     if (st != ASR_OK) return st;
@@ -102,8 +104,9 @@ asr_status launch_static_group(int dev, const TensorEntry *dev_table, uint64_t t
     return check_launch();
 }
 
-// Tensors that are not vector-eligible take the plain kernel, its table in
-// the launch parameters (staged in g_stage_plain, kCapLarge per launch).
+// Tensors whose buffers are not 16-byte aligned take the plain kernel, its
+// table in the launch parameters (staged in g_stage_plain, kCapLarge per
+// launch).
 template <int PT, int GT, int RM>
 asr_status launch_static_plain(int dev, const asr_tensor_desc *table, int32_t n_tensors, const AdamParams &P,
                                cudaStream_t stream)
@@ -115,7 +118,7 @@ asr_status launch_static_plain(int dev, const asr_tensor_desc *table, int32_t n_
         uint64_t tiles = 0;
         for (; i < n_tensors && c < kCapLarge; ++i) {
             const asr_tensor_desc &d = table[i];
-            if (d.n == 0 || d.param_dtype != PT || d.grad_dtype != GT || desc_fast(d)) continue;
+            if (d.n == 0 || d.param_dtype != PT || d.grad_dtype != GT || desc_class(d, RM) != kPlainPath) continue;
             TensorEntry &T = g_stage_plain.t[c++];
             T.p = d.param;
             T.g = d.grad;
@@ -129,7 +132,7 @@ asr_status launch_static_plain(int dev, const asr_tensor_desc *table, int32_t n_
         if (c == 0) continue;
         auto kernel = adamw_sr_kernel<PT, GT, RM, false, kCapLarge>;
         if (grid == 0) {
-            asr_status st = static_grid(kernel, dev, 6 + variant_slot(PT, GT, RM), kThreads, 0, &grid);
+            asr_status st = static_grid(kernel, dev, 12 + variant_slot(PT, GT, RM), kThreads, 0, &grid);
             if (st != ASR_OK) return st;
         }
         g_stage_plain.total_tiles = tiles;
@@ -142,14 +145,23 @@ asr_status launch_static_plain(int dev, const asr_tensor_desc *table, int32_t n_
     return ASR_OK;
 }
 
+// One dtype/rounding combination: its pipelined blocks of the static array
+// (block 0: bases that are multiples of 4, block 1: any base), then its
+// tensors with unaligned buffers.
 template <int PT, int GT, int RM>
-asr_status launch_static_combo(int dev, const TensorEntry *dev_table, uint64_t tiles, bool any_vector,
-                               const asr_tensor_desc *table, int32_t n_tensors, const AdamParams &P,
-                               cudaStream_t stream)
+asr_status launch_static_combo(int dev, const TensorEntry *const blocks[2], const uint64_t tiles[2],
+                               const int counts[2], const asr_tensor_desc *table, int32_t n_tensors,
+                               const AdamParams &P, cudaStream_t stream)
 {
-    if (any_vector) {
-        asr_status st = launch_static_group<PT, GT, RM>(dev, dev_table, tiles, P, stream);
+    if (counts[0] > 0) {
+        asr_status st = launch_static_group<PT, GT, RM, true>(dev, blocks[0], tiles[0], P, stream);
         if (st != ASR_OK) return st;
+    }
+    if constexpr (PT == ASR_BF16 && RM == ASR_ROUND_SR) {
+        if (counts[1] > 0) {
+            asr_status st = launch_static_group<PT, GT, RM, false>(dev, blocks[1], tiles[1], P, stream);
+            if (st != ASR_OK) return st;
+        }
     }
     return launch_static_plain<PT, GT, RM>(dev, table, n_tensors, P, stream);
 }
@@ -176,18 +188,20 @@ asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, con
     const int rm = static_cast<int>(hp->rounding);
 
     std::lock_guard<std::mutex> lk(g_stage_mu);
-    // Vector-eligible tensors: one contiguous block of the table per dtype
-    // group (group index = param dtype * 2 + grad dtype), sent in one copy.
+    // Tensors for the pipelined kernel: one contiguous block of the table per
+    // (dtype group, base class) -- block index 2 * (param dtype * 2 + grad
+    // dtype) + (base class is "any base") -- all sent in one copy.
     int used = 0;
-    int group_start[4] = {0, 0, 0, 0}, group_count[4] = {0, 0, 0, 0};
-    uint64_t group_tiles[4] = {0, 0, 0, 0};
-    for (int gi = 0; gi < 4; ++gi) {
-        const int pdt = gi / 2, gdt = gi % 2;
-        group_start[gi] = used;
+    int block_start[8] = {}, block_count[8] = {};
+    uint64_t block_tiles[8] = {};
+    for (int b = 0; b < 8; ++b) {
+        const int gi = b / 2, pdt = gi / 2, gdt = gi % 2;
+        const int cls = b % 2 ? kVecAnyBase : kVecA4;
+        block_start[b] = used;
         uint64_t tiles = 0;
         for (int32_t i = 0; i < n_tensors; ++i) {
             const asr_tensor_desc &d = table[i];
-            if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || !desc_fast(d)) continue;
+            if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || desc_class(d, rm) != cls) continue;
             TensorEntry &T = g_stage_table[used++];
             T.p = d.param;
             T.g = d.grad;
@@ -198,8 +212,8 @@ asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, con
             tiles += (d.n + tma_tile(pdt, gdt) - 1) / tma_tile(pdt, gdt);
             T.tile_end = tiles;
         }
-        group_count[gi] = used - group_start[gi];
-        group_tiles[gi] = tiles;
+        block_count[b] = used - block_start[b];
+        block_tiles[b] = tiles;
     }
     if (used > 0) {
         // From pageable host memory: returns once the table is staged for the
@@ -209,21 +223,21 @@ asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, con
         if (e != cudaSuccess) return cuda_fail(e);
     }
     for (int gi = 0; gi < 4; ++gi) {
-        const bool any = group_count[gi] > 0;
-        const TensorEntry *tb = dev_table + group_start[gi];
-        const uint64_t tl = group_tiles[gi];
+        const TensorEntry *const blocks[2] = {dev_table + block_start[2 * gi], dev_table + block_start[2 * gi + 1]};
+        const uint64_t tiles[2] = {block_tiles[2 * gi], block_tiles[2 * gi + 1]};
+        const int counts[2] = {block_count[2 * gi], block_count[2 * gi + 1]};
         if (gi == 3)        // bf16 params, bf16 grads
             st = rm == ASR_ROUND_SR
-                ? launch_static_combo<ASR_BF16, ASR_BF16, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream)
-                : launch_static_combo<ASR_BF16, ASR_BF16, ASR_ROUND_RNE>(dev, tb, tl, any, table, n_tensors, P, stream);
+                ? launch_static_combo<ASR_BF16, ASR_BF16, ASR_ROUND_SR>(dev, blocks, tiles, counts, table, n_tensors, P, stream)
+                : launch_static_combo<ASR_BF16, ASR_BF16, ASR_ROUND_RNE>(dev, blocks, tiles, counts, table, n_tensors, P, stream);
         else if (gi == 2)   // bf16 params, f32 grads
             st = rm == ASR_ROUND_SR
-                ? launch_static_combo<ASR_BF16, ASR_F32, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream)
-                : launch_static_combo<ASR_BF16, ASR_F32, ASR_ROUND_RNE>(dev, tb, tl, any, table, n_tensors, P, stream);
+                ? launch_static_combo<ASR_BF16, ASR_F32, ASR_ROUND_SR>(dev, blocks, tiles, counts, table, n_tensors, P, stream)
+                : launch_static_combo<ASR_BF16, ASR_F32, ASR_ROUND_RNE>(dev, blocks, tiles, counts, table, n_tensors, P, stream);
         else if (gi == 1)   // f32 params, bf16 grads (the rounding mode does not apply)
-            st = launch_static_combo<ASR_F32, ASR_BF16, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream);
+            st = launch_static_combo<ASR_F32, ASR_BF16, ASR_ROUND_SR>(dev, blocks, tiles, counts, table, n_tensors, P, stream);
         else                // f32 params, f32 grads
-            st = launch_static_combo<ASR_F32, ASR_F32, ASR_ROUND_SR>(dev, tb, tl, any, table, n_tensors, P, stream);
+            st = launch_static_combo<ASR_F32, ASR_F32, ASR_ROUND_SR>(dev, blocks, tiles, counts, table, n_tensors, P, stream);
         if (st != ASR_OK) return st;
     }
     return ASR_OK;

@@ -1,6 +1,7 @@
 """Edge cases at the largest sizes the entry points take: one tensor longer
-than 2^32 elements (offsets inside a single tensor past 32 bits, on both the
-pipelined and the plain kernel) and a GEMM with M = 2^24 rows, the limit.
+than 2^32 elements (offsets inside a single tensor past 32 bits, on both
+forms of the pipelined kernel and on the plain kernel) and a GEMM with
+M = 2^24 rows, the limit.
 Windows and rows are checked against the oracle bit for bit."""
 import numpy as np
 import pytest
@@ -24,22 +25,25 @@ def asr():
 def test_single_tensor_longer_than_2_32(asr, orc):
     """n = 2^32 + 37 bf16 params with bf16 grads and f32 moments (51.5 GB):
     step 1 at base_index 8 (16-byte-aligned, base % 4 == 0: the pipelined
-    kernel), step 2 from that state at base_index 5 (the plain kernel).  The
-    first elements, the 4,096 around element 2^32 and the ragged end match
-    the oracle run on the same windows with their base indices."""
+    kernel), step 2 from that state at base_index 5 (the pipelined kernel
+    drawing three counters per unit), step 3 on the same buffers seen one
+    element later (not 16-byte aligned: the plain kernel).  The first
+    elements, the 4,096 around element 2^32 and the ragged end match the
+    oracle run on the same windows with their base indices."""
     import torch
     n = 2 ** 32 + 37
-    p = torch.empty(n, dtype=torch.bfloat16, device="cuda")
-    g = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    P = torch.empty(n + 1, dtype=torch.bfloat16, device="cuda")
+    G = torch.empty(n + 1, dtype=torch.bfloat16, device="cuda")
     gen = torch.Generator(device="cuda")
     gen.manual_seed(77)
-    p.normal_(0.0, 0.02, generator=gen)
-    g.normal_(0.0, 1e-3, generator=gen)
-    m = torch.zeros(n, dtype=torch.float32, device="cuda")
-    v = torch.zeros(n, dtype=torch.float32, device="cuda")
+    P.normal_(0.0, 0.02, generator=gen)
+    G.normal_(0.0, 1e-3, generator=gen)
+    M = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
+    V = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
     windows = [(0, 4096), (2 ** 32 - 2048, 2 ** 32 + 2048), (n - 4133, n)]
     try:
-        for step, base in ((1, 8), (2, 5)):
+        for step, base, shift in ((1, 8, 0), (2, 5, 0), (3, 8, 1)):
+            p, g, m, v = (t[shift:shift + n] for t in (P, G, M, V))
             before = [(host(p[lo:hi]), host(g[lo:hi]), host(m[lo:hi]), host(v[lo:hi])) for lo, hi in windows]
             asr.asr_adamw_sr_step(p, g, m, v, step=step, seed=2 ** 40 + 3, base_index=base, **HP)
             torch.cuda.synchronize()
@@ -50,7 +54,7 @@ def test_single_tensor_longer_than_2_32(asr, orc):
                 assert_same_bits(host(v[lo:hi]), vh, f"step {step} v[{lo}:{hi}]")
         assert asr.asr_take_device_error() == 0
     finally:
-        del p, g, m, v
+        del P, G, M, V
         torch.cuda.empty_cache()
 
 

@@ -134,6 +134,44 @@ def test_llama_param_set_sampled(asr, orc, shape, steps, checked):
     torch.cuda.empty_cache()
 
 
+def test_llama_set_at_positions_off_a_multiple_of_4(asr, orc):
+    """A Llama-shaped set (the leading tensors of the 1.5B layout, ~300M
+    params, 16-byte-aligned buffers) whose global positions are shifted by
+    1, 2 or 3 per tensor, as when an odd-sized parameter comes earlier in a
+    model: every tensor then takes the pipelined kernel that draws three
+    Philox counters per 8-element unit.  Sampled windows of every tensor
+    equal the oracle at steps 1 and 3."""
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    ps = W.DeviceParamSet(W.LLAMA_1B, seed=5, max_params=300_000_000)
+    shift = [1 + (t % 3) for t in range(len(ps.sizes))]
+    tensors = [(p, g, m, v, base + shift[t]) for t, (p, g, m, v, base) in enumerate(ps.tensors())]
+    assert all(b % 4 != 0 for *_, b in tensors)
+    table = _lib.make_table(tensors)
+    rng = np.random.default_rng(32)
+    windows = pick_windows(rng, ps.sizes, per_tensor=2, length=2048)
+    for step in (1, 2, 3):
+        if step > 1:
+            ps.new_grads()
+        before = []
+        if step != 2:
+            for t, st, n in windows:
+                a = ps.starts[t] + st
+                before.append([host(x[a:a + n]) for x in (ps.p, ps.g, ps.m, ps.v)])
+        asr.asr_adamw_sr_multi_tensor(table, step=step, seed=9, device=ps.device, **HP)
+        torch.cuda.synchronize()
+        for (t, st, n), (p, g, m, v) in zip(windows, before):
+            a = ps.starts[t] + st
+            orc.adamw_step(p, g, m, v, step=step, seed=9, base_index=a + shift[t], **HP)
+            where = f"{ps.table[t][0]}[{st}:{st + n}] step {step}"
+            assert_same_bits(host(ps.p[a:a + n]), p, where + " p")
+            assert_same_bits(host(ps.m[a:a + n]), m, where + " m")
+            assert_same_bits(host(ps.v[a:a + n]), v, where + " v")
+    assert asr.asr_take_device_error() == 0
+    del ps
+    torch.cuda.empty_cache()
+
+
 def test_concurrent_calls_from_threads_and_streams(asr, orc):
     """Two host threads, each with its own stream and its own tensor set,
     issue 5 multi-tensor steps each with no synchronisation between them (the
