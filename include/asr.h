@@ -17,8 +17,9 @@
  *     cudaMalloc / torch CUDA memory, managed memory), owned by the caller.
  *     The library allocates no memory at run time.  What it keeps between
  *     calls: per-device caches of launch shapes (and the tensor-map encoder's
- *     address), a 4-byte device error word (asr_take_device_error) and the
- *     static descriptor array of asr_adamw_sr_multi_tensor_static.
+ *     address), a 4-byte device error word with a 4-byte copy slot
+ *     (asr_take_device_error) and the static descriptor array of
+ *     asr_adamw_sr_multi_tensor_static.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising the host.  Buffers
  *     must stay valid until the stream reaches the work.
@@ -30,8 +31,11 @@
  *     synchronising CUDA call of the caller.
  *   - n == 0 is a valid no-op (pointers may then be NULL).
  *   - The element-wise entry points (Philox, rounding, AdamW) accept any
- *     element alignment; 16-byte-aligned buffers and a base_index that is a
- *     multiple of 4 take the vectorised fast path.  The GEMM states its own
+ *     element alignment.  The AdamW step takes its pipelined path for every
+ *     tensor whose buffers are 16-byte aligned (a base_index that is not a
+ *     multiple of 4 costs one more Philox call per 8 elements); the
+ *     rounding op's vectorised path wants 16-byte-aligned buffers and a
+ *     base_index that is a multiple of 4.  The GEMM states its own
  *     requirements.
  *   - Buffers of one call must not overlap each other (not checked).
  *   - The library is thread-safe; calls on different streams may run
@@ -157,8 +161,8 @@ asr_status asr_adamw_sr_step(void *param, int32_t pdt, const void *grad, int32_t
                              uint64_t base_index, const asr_adamw_hparams *hp,
                              asr_stream_t stream);
 
-/* The same step over many tensors in one grid-stride launch per dtype
- * combination ("adamw-sr", Method: one global parameter position per
+/* The same step over many tensors in one launch per dtype combination
+ * (and kernel path) ("adamw-sr", Method: one global parameter position per
  * element).  Bitwise equal to calling asr_adamw_sr_step on each descriptor in
  * turn.  table: HOST array of n_tensors descriptors (read during the call
  * only); n_tensors >= 0.  Descriptors with n == 0 are skipped. */
