@@ -105,3 +105,64 @@ def test_shard_pieces_cover_range():
         for t, off, n, base in pieces:
             assert base == pos and 0 <= off and off + n <= SIZES[t]
             pos += n
+
+
+def _optim_rank_main(rank, world, port, out_dir):
+    """One rank: an AdamWSR over the pieces of its share of the flat vector
+    (cut on any element, align=1), numbered from the share's start."""
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import torch
+    import torch.distributed as dist
+
+    from stochastic_rounding_gb300.optim import AdamWSR
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    start, end = sharding.shard_bounds(sum(SIZES), world, rank, align=1)
+    pieces = sharding.shard_pieces(SIZES, start, end)
+    params = [torch.nn.Parameter(torch.zeros(n, dtype=torch.bfloat16)) for _, _, n, _ in pieces]
+    opt = AdamWSR(params, base_offset=start)
+    mine = [(t, off, n, opt.base_index(p)) for (t, off, n, _), p in zip(pieces, params)]
+    gathered = [None] * world
+    dist.all_gather_object(gathered, mine)
+    if rank == 0:
+        import json
+        with open(os.path.join(out_dir, "positions.json"), "w") as f:
+            json.dump(gathered, f)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_rank_local_optimizers_number_like_the_whole(tmp_path):
+    """Three gloo ranks, each holding an AdamWSR over its share of the flat
+    parameter vector cut at arbitrary elements and given the share's start
+    as base_offset: every piece's global position equals the position of the
+    same elements in one optimizer over the whole model, and the pieces tile
+    the vector exactly once."""
+    import json
+
+    import torch
+    import torch.multiprocessing as mp
+
+    from stochastic_rounding_gb300.optim import AdamWSR
+    world = 3
+    mp.start_processes(_optim_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       start_method="spawn", join=True)
+    with open(tmp_path / "positions.json") as f:
+        gathered = json.load(f)
+    whole = AdamWSR([torch.nn.Parameter(torch.zeros(n, dtype=torch.bfloat16)) for n in SIZES])
+    starts = [whole.base_index(p) for p in whole.param_groups[0]["params"]]
+    seen = []
+    for rank_pieces in gathered:
+        for t, off, n, pos in rank_pieces:
+            assert pos == starts[t] + off
+            seen.append((pos, n))
+    seen.sort()
+    covered = 0
+    for pos, n in seen:
+        assert pos == covered
+        covered += n
+    assert covered == sum(SIZES)
+    assert any(pos % 4 for pos, _ in seen), "expected cuts off a multiple of 4"
