@@ -42,6 +42,13 @@
  *     concurrently on disjoint buffers.  One exception:
  *     asr_adamw_sr_multi_tensor_static keeps its table in one shared device
  *     array, so its calls must not overlap one another on the GPU.
+ *   - CUDA graphs: asr_philox4x32, asr_stochastic_round_bf16,
+ *     asr_adamw_sr_step, asr_adamw_sr_multi_tensor and asr_gemm_bf16_sr may
+ *     be captured into a graph (stream capture) once a call of the same
+ *     entry point has run on the device outside any capture -- that first
+ *     call sets up the device's cached launch shapes -- and a replay gives
+ *     the bits the direct calls give.  asr_take_device_error waits for its
+ *     stream and is not for capture; asr_take_device_error_async is.
  *   - The kernels are built for sm_103a (GB300) only; on any other GPU the
  *     first launch fails and the call returns ASR_ERR_CUDA.
  *
