@@ -560,12 +560,13 @@ def run_gpu(args):
     done_out = [None] * len(chunks)          # params of chunk c copied out (params free)
     launches_e2e = 0
 
-    def e2e_steps(count):
+    def e2e_steps(count, compute=True):
         nonlocal t_global, launches_e2e
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
         for _ in range(count):
-            t_global += 1
+            if compute:
+                t_global += 1
             for c, (lo, hi, ctable) in enumerate(chunks):
                 ev_in = torch.cuda.Event()
                 with torch.cuda.stream(s_in):
@@ -576,8 +577,9 @@ def run_gpu(args):
                 stream.wait_event(ev_in)
                 if done_out[c] is not None:
                     stream.wait_event(done_out[c])
-                asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
-                launches_e2e += 1
+                if compute:
+                    asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
+                    launches_e2e += 1
                 ev_c = torch.cuda.Event()
                 ev_c.record(stream)
                 done_cmp[c] = ev_c
@@ -605,6 +607,16 @@ def run_gpu(args):
     require_no_device_error(asr.asr_take_device_error, "timed end-to-end steps")
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
+    # the same pipeline with the step calls left out (copies and their
+    # ordering only), outside the timed region: what this machine's host link
+    # allows for the same transfers
+    c_start = torch.cuda.Event(enable_timing=True)
+    c_end = torch.cuda.Event(enable_timing=True)
+    c_start.record(stream)
+    e2e_steps(e_steps, compute=False)
+    c_end.record(stream)
+    torch.cuda.synchronize(dev)
+    copies_value = world * n * e_steps / (max_over_ranks(c_start.elapsed_time(c_end)) / 1e3) / 1e9
     del g_host, p_host
     link = host_link_rates(dev)
     # the copies alone bound the end-to-end step: 2n bytes in and 2n out
@@ -641,6 +653,7 @@ def run_gpu(args):
                     "gpu_launches": launches_e2e,
                     "link_gbs": link, "link_floor_gparams_s": n / floor_s / 1e9,
                     "frac_of_link_floor": e2e_value / world / (n / floor_s / 1e9),
+                    "copies_only_gparams_s": copies_value, "frac_of_copies_only": e2e_value / copies_value,
                     "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host; "
                             "chunks of consecutive tensors pipelined over three streams"},
             "gpu_launches": launches,
