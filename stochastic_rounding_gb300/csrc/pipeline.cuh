@@ -27,20 +27,25 @@
 #define ASR_TMA_EVICT_FIRST 1
 #endif
 
-// Pipeline shape per (param, grad) dtype: the number of consumer warps, one
-// 8-element unit per consumer thread per tile, and as many stages (at most
+// Pipeline shape per (param, grad) dtype: the number of consumer warps, the
+// 8-element units per consumer thread per tile, and as many stages (at most
 // four) as fit in a 224 KB shared-memory budget.  Measured on GB300 with the
-// dynamic tile schedule, all shapes in the same run, two repetitions (GB/s;
-// bf16/bf16 on the Llama-3-8B set, the others on one 268M-element tensor):
-//   bf16/bf16: 24 warps, 3 stages of 72 KB: 7,078-7,088 (20 warps, 3 stages
-//              in 200 KB: 6,866-6,905; 24 warps, 2 stages: 7,031-7,034;
-//              16 warps: 6,443) -- the most arithmetic per byte (Philox and
-//              rounding), so the most warps;
+// dynamic tile schedule, all shapes in the same run, two or three repetitions
+// (GB/s; bf16/bf16 on the Llama-3-8B set, the others on one 268M-element
+// tensor):
+//   bf16/bf16: 16 warps x 2 units (8,192-element tiles), 2 stages of 96 KB:
+//              7,179-7,183 (24 warps x 1 unit, 3 stages of 72 KB:
+//              7,078-7,088; 14 x 2: 6,308; 18 x 2: 7,007; 10 x 3: 5,141;
+//              8 x 4: 4,480; 20 x 1 in 200 KB: 6,866-6,905) -- the most
+//              arithmetic per byte (Philox and rounding): two independent
+//              units per thread beat more warps;
 //   bf16/f32:  20 warps, 3 stages: 7,073-7,080 (16: 6,533-6,626; 24: 7,033-7,042);
 //   f32/bf16:  16 warps, 4 stages: 7,021-7,031 (12: 6,962-6,968);
 //   f32/f32:   12 warps, 4 stages: 7,066-7,075 (16: 7,022).
+// Two units per thread lose for the other three (bf16/f32 20 x 1 -> 10 x 2:
+// 5,358; f32/bf16 16 x 1 -> 8 x 2: 5,999; f32/f32 12 x 1 -> 6 x 2: 4,886).
 #ifndef ASR_TMA_WARPS_BB
-#define ASR_TMA_WARPS_BB 24             // bf16 params, bf16 grads
+#define ASR_TMA_WARPS_BB 16             // bf16 params, bf16 grads (two units per thread)
 #endif
 #ifndef ASR_TMA_WARPS_BF
 #define ASR_TMA_WARPS_BF 20             // bf16 params, f32 grads
@@ -50,6 +55,9 @@
 #endif
 #ifndef ASR_TMA_WARPS_FF
 #define ASR_TMA_WARPS_FF 12             // f32 params, f32 grads
+#endif
+#ifndef ASR_TMA_UNITS_BB
+#define ASR_TMA_UNITS_BB 2              // units per consumer thread, bf16 params and grads
 #endif
 template <int PT, int GT>
 struct TmaShape {
@@ -61,7 +69,12 @@ struct TmaShape {
 #endif
     static constexpr int kConsumers = kWarps * 32;
     static constexpr int kThreads = kConsumers + 32;        // + one producer warp
-    static constexpr int kUnits = 1;                        // 8-element units per consumer thread per tile
+#ifdef ASR_TMA_UNITS
+    static constexpr int kUnits = ASR_TMA_UNITS;            // one shape for all, for sweeps
+#else
+    // 8-element units per consumer thread per tile
+    static constexpr int kUnits = PT == ASR_BF16 ? (GT == ASR_BF16 ? ASR_TMA_UNITS_BB : 1) : 1;
+#endif
     static constexpr int kTile = kConsumers * kVec * kUnits;
 };
 

@@ -99,10 +99,11 @@ def test_unaligned_buffers(asr, orc, off):
     torch.cuda.synchronize()
 
 
-# Edges of the pipelined kernel's tiles: 256 elements per consumer warp, 12
-# to 24 warps by dtype combination, so every multiple of 1,024 from 3,072 to
-# 6,144 elements is some combination's tile; one and two tiles, +-1.
-TILE_EDGES = sorted({t * k + d for t in (3072, 4096, 5120, 6144) for k in (1, 2) for d in (-1, 0, 1)})
+# Edges of the pipelined kernel's tiles: 256 elements per consumer warp and
+# unit, 3,072 to 8,192 elements by dtype combination (multiples of 1,024
+# from 3,072 to 6,144 and 8,192 cover every shape in use or in the sweeps);
+# one and two tiles, +-1.
+TILE_EDGES = sorted({t * k + d for t in (3072, 4096, 5120, 6144, 8192) for k in (1, 2) for d in (-1, 0, 1)})
 
 
 @pytest.mark.parametrize("pdt,gdt", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f32")])
