@@ -42,8 +42,10 @@
 //   bf16/f32:  20 warps, 3 stages: 7,073-7,080 (16: 6,533-6,626; 24: 7,033-7,042);
 //   f32/bf16:  16 warps, 4 stages: 7,021-7,031 (12: 6,962-6,968);
 //   f32/f32:   12 warps, 4 stages: 7,066-7,075 (16: 7,022).
-// Two units per thread lose for the other three (bf16/f32 20 x 1 -> 10 x 2:
-// 5,358; f32/bf16 16 x 1 -> 8 x 2: 5,999; f32/f32 12 x 1 -> 6 x 2: 4,886).
+// Two units per thread lose for the other three (bf16/f32 10 x 2: 5,358,
+// 12 x 2: 6,288, 16 x 2: 7,061 against 20 x 1: 7,091; f32/bf16 8 x 2: 5,999,
+// 12 x 2: 7,013 against 16 x 1: 7,025; f32/f32 6 x 2: 4,886, 8 x 2: 6,378,
+// 12 x 2: 7,004 against 12 x 1: 7,078).
 #ifndef ASR_TMA_WARPS_BB
 #define ASR_TMA_WARPS_BB 16             // bf16 params, bf16 grads (two units per thread)
 #endif
@@ -59,6 +61,15 @@
 #ifndef ASR_TMA_UNITS_BB
 #define ASR_TMA_UNITS_BB 2              // units per consumer thread, bf16 params and grads
 #endif
+#ifndef ASR_TMA_UNITS_BF
+#define ASR_TMA_UNITS_BF 1
+#endif
+#ifndef ASR_TMA_UNITS_FB
+#define ASR_TMA_UNITS_FB 1
+#endif
+#ifndef ASR_TMA_UNITS_FF
+#define ASR_TMA_UNITS_FF 1
+#endif
 template <int PT, int GT>
 struct TmaShape {
 #ifdef ASR_TMA_WARPS
@@ -73,7 +84,8 @@ struct TmaShape {
     static constexpr int kUnits = ASR_TMA_UNITS;            // one shape for all, for sweeps
 #else
     // 8-element units per consumer thread per tile
-    static constexpr int kUnits = PT == ASR_BF16 ? (GT == ASR_BF16 ? ASR_TMA_UNITS_BB : 1) : 1;
+    static constexpr int kUnits = PT == ASR_BF16 ? (GT == ASR_BF16 ? ASR_TMA_UNITS_BB : ASR_TMA_UNITS_BF)
+                                                 : (GT == ASR_BF16 ? ASR_TMA_UNITS_FB : ASR_TMA_UNITS_FF);
 #endif
     static constexpr int kTile = kConsumers * kVec * kUnits;
 };
