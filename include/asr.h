@@ -33,9 +33,8 @@
  *   - The element-wise entry points (Philox, rounding, AdamW) accept any
  *     element alignment.  The AdamW step takes its pipelined path for every
  *     tensor whose buffers are 16-byte aligned (a base_index that is not a
- *     multiple of 4 costs one more Philox call per 8 elements); the
- *     rounding op's vectorised path wants 16-byte-aligned buffers and a
- *     base_index that is a multiple of 4.  The GEMM states its own
+ *     multiple of 4 costs one more Philox call per 8 elements); so does
+ *     the rounding op's vectorised path.  The GEMM states its own
  *     requirements.
  *   - Buffers of one call must not overlap each other (not checked).
  *   - The library is thread-safe; calls on different streams may run

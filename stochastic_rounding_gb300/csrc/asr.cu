@@ -487,10 +487,14 @@ asr_status asr_stochastic_round_bf16(const float *x, const uint32_t *rbits, uint
     P.base = base_index;
     P.step = step;
     P.keys = make_keys(seed);
-    const bool fast = aligned16(x) && aligned16(out) && (!rbits || aligned16(rbits)) && (base_index & 3u) == 0;
+    // vector loads and stores wherever the buffers are 16-byte aligned; a
+    // base off a multiple of 4 only costs a third Philox call per unit
+    const bool fast = aligned16(x) && aligned16(out) && (!rbits || aligned16(rbits));
+    const bool a4 = (base_index & 3u) == 0;
     void (*kernel)(const SrParams) = nullptr;
     if (rbits) kernel = fast ? sr_bf16_kernel<true, true> : sr_bf16_kernel<false, true>;
-    else kernel = fast ? sr_bf16_kernel<true, false> : sr_bf16_kernel<false, false>;
+    else if (!fast) kernel = sr_bf16_kernel<false, false>;
+    else kernel = a4 ? sr_bf16_kernel<true, false, true> : sr_bf16_kernel<true, false, false>;
     int grid = 0;
     asr_status st = persistent_grid(kernel, &grid);
     if (st != ASR_OK) return st;

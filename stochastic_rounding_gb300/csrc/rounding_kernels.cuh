@@ -13,8 +13,9 @@ struct SrParams {
     RoundKeys keys;
 };
 
-// FAST: x/out (and rbits) 16-byte aligned, base % 4 == 0.
-template <bool FAST, bool RBITS>
+// FAST: x/out (and rbits) 16-byte aligned.  A4: base % 4 == 0, so each
+// 8-element unit's words come from two Philox counters (three otherwise).
+template <bool FAST, bool RBITS, bool A4 = true>
 __global__ void __launch_bounds__(kThreads) sr_bf16_kernel(const __grid_constant__ SrParams P)
 {
     const uint64_t units = (P.n + kVec - 1) / kVec;
@@ -29,7 +30,7 @@ __global__ void __launch_bounds__(kThreads) sr_bf16_kernel(const __grid_constant
                 r[0] = ra.x; r[1] = ra.y; r[2] = ra.z; r[3] = ra.w;
                 r[4] = rb.x; r[5] = rb.y; r[6] = rb.z; r[7] = rb.w;
             } else {
-                unit_words<true>(P.base, e, P.step, P.keys, r);
+                unit_words<A4>(P.base, e, P.step, P.keys, r);
             }
             const uint32_t xs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             uint32_t w[4];
