@@ -336,6 +336,7 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
     single("single_65536_bf16", 65536, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM,
            "1.4 MB: L2-resident and launch-bound")
     out["single_65536_bf16"]["host_us_per_call"] = binding_host_cost(asr, W, dev, gen)
+    out["single_65536_bf16"]["graph_us_per_step"] = graph_step_cost(asr, W, dev, gen)
     single("fp32_16777216", 16777216, torch.float32, torch.float32, 28, "fp32 params and grads")
     single("bf16_268435456", 268435456, torch.bfloat16, torch.bfloat16, BYTES_PER_PARAM, "one tensor")
     ps = W.DeviceParamSet(W.LLAMA_1B, device=dev, seed=2)
@@ -391,6 +392,34 @@ def optimizer_step_time(asr, tensors, dev, steps, warmup, n):
     out["note"] = ("AdamWSR.step() on the 8B set (291 parameters), wall clock with a synchronize at the end; "
                    "the blocking check waits for each step, the deferred one reads the error word one step late")
     return out
+
+
+def graph_step_cost(asr, W, dev, gen, n=65536, steps=50):
+    """GPU time per step of the small single-tensor step when its launches
+    come from a CUDA graph (50 consecutive steps captured once after an
+    ordinary call, then replayed): the cost of the step itself, without the
+    host's per-call work."""
+    import torch
+    p = W.device_normal_(torch.empty(n, dtype=torch.bfloat16, device=dev), gen, 0.02)
+    g = W.device_normal_(torch.empty(n, dtype=torch.bfloat16, device=dev), gen, 1e-3)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    asr.asr_adamw_sr_step(p, g, m, v, step=1, seed=0, **HP)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for t in range(2, steps + 2):
+            asr.asr_adamw_sr_step(p, g, m, v, step=t, seed=0, **HP)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    require_no_device_error(asr.asr_take_device_error, "graph-replayed steps")
+    return e0.elapsed_time(e1) / steps * 1e3
 
 
 def binding_host_cost(asr, W, dev, gen, n=65536, calls=200):
