@@ -32,9 +32,11 @@
  *   - n == 0 is a valid no-op (pointers may then be NULL).
  *   - The element-wise entry points (Philox, rounding, AdamW) accept any
  *     element alignment.  The AdamW step takes its pipelined path for every
- *     tensor whose buffers are 16-byte aligned (a base_index that is not a
- *     multiple of 4 costs one more Philox call per 8 elements); so does
- *     the rounding op's vectorised path.  The GEMM states its own
+ *     tensor whose buffers are 16-byte aligned, and for the part of a
+ *     tensor from its first element at which all four buffers are (the few
+ *     elements before that take a scalar path); a base_index that is not a
+ *     multiple of 4 costs one more Philox call per 8 elements, as it does
+ *     on the rounding op's vectorised path.  The GEMM states its own
  *     requirements.
  *   - Buffers of one call must not overlap each other (not checked).
  *   - The library is thread-safe; calls on different streams may run

@@ -196,6 +196,37 @@ int desc_class(const asr_tensor_desc &d, int rounding)
     return ASR_USE_TMA ? kVecAnyBase : kPlainPath;
 }
 
+// A descriptor whose buffers are not all 16-byte aligned, split where they
+// all become aligned: a head of h < 8 elements (the plain kernel) and the
+// rest from element h on, its base index advanced by h (a pipelined kernel).
+// Such an h exists whenever the four buffers are off alignment by amounts
+// that agree -- views of slices that start at the same element offset in
+// aligned storage, for instance.  Every element keeps its own global index,
+// so the split changes no bit.  Writes 1 or 2 descriptors to out.
+int split_unaligned(const asr_tensor_desc &d, int rounding, asr_tensor_desc out[2])
+{
+    out[0] = d;
+    if (d.n == 0 || desc_class(d, rounding) != kPlainPath) return 1;
+    const uintptr_t ps = d.param_dtype == ASR_BF16 ? 2 : 4, gs = d.grad_dtype == ASR_BF16 ? 2 : 4;
+    for (uint64_t h = 1; h < 8 && h < d.n; ++h) {
+        const uintptr_t p = reinterpret_cast<uintptr_t>(d.param) + h * ps;
+        const uintptr_t g = reinterpret_cast<uintptr_t>(d.grad) + h * gs;
+        const uintptr_t m = reinterpret_cast<uintptr_t>(d.exp_avg + h);
+        const uintptr_t v = reinterpret_cast<uintptr_t>(d.exp_avg_sq + h);
+        if (((p | g | m | v) & 15u) != 0) continue;
+        out[0].n = h;
+        out[1] = d;
+        out[1].param = reinterpret_cast<void *>(p);
+        out[1].grad = reinterpret_cast<const void *>(g);
+        out[1].exp_avg = d.exp_avg + h;
+        out[1].exp_avg_sq = d.exp_avg_sq + h;
+        out[1].n = d.n - h;
+        out[1].base_index = d.base_index + h;
+        return 2;
+    }
+    return 1;
+}
+
 // Dynamic shared memory opt-in and persistent grid of the bulk-copy kernel,
 // cached per (device, kernel).
 template <typename K>
@@ -338,9 +369,19 @@ asr_status run_adamw(const asr_tensor_desc *table, int32_t n_tensors, const asr_
     P.keys = make_keys(hp->seed);
     P.step = hp->step;
 
-    // Group by (param dtype, grad dtype, kernel class), keeping order.
-    // Every element is independent, so the grouping cannot change any bit.
-    const int nt = n_tensors;
+    // Split unaligned tensors at their first common aligned element, then
+    // group by (param dtype, grad dtype, kernel class), keeping order.  Every
+    // element is independent, so neither step can change any bit.
+    const int rm = static_cast<int>(hp->rounding);
+    asr_tensor_desc small[8];
+    std::unique_ptr<asr_tensor_desc[]> split_holder;
+    asr_tensor_desc *split = small;
+    if (2 * static_cast<int64_t>(n_tensors) > 8) {
+        split_holder.reset(new asr_tensor_desc[2 * static_cast<size_t>(n_tensors)]);
+        split = split_holder.get();
+    }
+    int nt = 0;
+    for (int32_t i = 0; i < n_tensors; ++i) nt += split_unaligned(table[i], rm, split + nt);
     const asr_tensor_desc **sel = nullptr;
     const asr_tensor_desc *one[1];
     std::unique_ptr<const asr_tensor_desc *[]> holder;
@@ -350,13 +391,12 @@ asr_status run_adamw(const asr_tensor_desc *table, int32_t n_tensors, const asr_
         holder.reset(new const asr_tensor_desc *[nt]);
         sel = holder.get();
     }
-    const int rm = static_cast<int>(hp->rounding);
     for (int pdt = 0; pdt < 2; ++pdt)
         for (int gdt = 0; gdt < 2; ++gdt)
             for (int cls = kPlainPath; cls <= kVecAnyBase; ++cls) {
                 int c = 0;
                 for (int i = 0; i < nt; ++i) {
-                    const asr_tensor_desc &d = table[i];
+                    const asr_tensor_desc &d = split[i];
                     if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || desc_class(d, rm) != cls)
                         continue;
                     sel[c++] = &d;

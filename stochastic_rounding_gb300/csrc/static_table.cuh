@@ -80,8 +80,11 @@ asr_status static_grid(K kernel, int dev, int slot, int threads, int smem, int *
 
 constexpr int variant_slot(int pdt, int gdt, int rm) { return pdt == ASR_BF16 ? gdt * 2 + rm : 4 + gdt; }
 
-// Host staging: fixed arrays, guarded by a mutex for the duration of a call.
+// Host staging: fixed arrays, guarded by a mutex for the duration of a call:
+// the descriptors after splitting unaligned tensors (split_unaligned), the
+// pipelined kernels' table and the plain kernel's launch table.
 std::mutex g_stage_mu;
+asr_tensor_desc g_stage_split[2 * kStaticTableMax];
 TensorEntry g_stage_table[kStaticTableMax];
 AdamTable<kCapLarge> g_stage_plain;
 
@@ -188,6 +191,12 @@ asr_status run_adamw_static(const asr_tensor_desc *table, int32_t n_tensors, con
     const int rm = static_cast<int>(hp->rounding);
 
     std::lock_guard<std::mutex> lk(g_stage_mu);
+    // unaligned tensors split at their first common aligned element; from
+    // here on the split descriptors stand for the caller's table
+    int32_t n_split = 0;
+    for (int32_t i = 0; i < n_tensors; ++i) n_split += split_unaligned(table[i], rm, g_stage_split + n_split);
+    table = g_stage_split;
+    n_tensors = n_split;
     // Tensors for the pipelined kernel: one contiguous block of the table per
     // (dtype group, base class) -- block index 2 * (param dtype * 2 + grad
     // dtype) + (base class is "any base") -- all sent in one copy.

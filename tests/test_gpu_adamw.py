@@ -82,8 +82,10 @@ def test_dtype_combinations_ragged(asr, orc, pdt, gdt, rounding, base):
 
 @pytest.mark.parametrize("off", [1, 2, 3])
 def test_unaligned_buffers(asr, orc, off):
-    """Buffers that start off a 16-byte boundary (slices) take the scalar
-    path and still match bit for bit; nothing outside the slice is written."""
+    """Buffers that start off a 16-byte boundary by the same element offset
+    (slices) are split at the first element where all four are aligned: a
+    scalar head, then the pipelined kernel.  Bit-exact; nothing outside the
+    slice is written."""
     import torch
     n = 4096 * 2 + 77
     rng = np.random.default_rng(off)
@@ -96,6 +98,34 @@ def test_unaligned_buffers(asr, orc, off):
     _check(hs, d, f"offset {off}")
     for g0, t in zip(guard, full):
         assert np.array_equal(host(t)[:off], g0)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("pdt,gdt", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f32")])
+@pytest.mark.parametrize("offs", [(1, 1, 1, 1), (3, 3, 3, 3), (7, 7, 7, 7), (1, 3, 1, 1), (1, 1, 2, 2), (0, 0, 1, 1),
+                                  (2, 2, 3, 3)])
+def test_unaligned_views(asr, orc, pdt, gdt, offs):
+    """p, g, m, v each a view some elements into its storage, in every dtype
+    combination: where some element puts all four on a 16-byte boundary the
+    tensor is split there (scalar head, pipelined rest), where none does it
+    takes the plain kernel -- either way bit-exact against the oracle, with
+    guard words before and after every view untouched."""
+    import torch
+    rng = np.random.default_rng(sum(offs) + 7)
+    n = 2 * 8192 + 45
+    h = _make(rng, n, pdt, gdt)
+    fulls, views = [], []
+    for a, off in zip(h, offs):
+        guard = np.full(off + 9, 0x7E, a.dtype)
+        full = dev(np.concatenate([guard[:off], a, guard[off:]]))
+        fulls.append((full, off))
+        views.append(full[off:off + n])
+    for base in (12, 13):
+        _step_both(asr, orc, h, views, step=2, seed=8, base_index=base, **HP)
+        _check(h, views, f"{pdt}/{gdt} offsets {offs} base {base}")
+    for full, off in fulls:
+        t = host(full)
+        assert np.all(t[:off] == 0x7E) and np.all(t[off + n:] == 0x7E), f"offsets {offs}: wrote outside the view"
     torch.cuda.synchronize()
 
 
@@ -342,27 +372,33 @@ def test_error_bits_taken_without_waiting(asr):
 def test_pipeline_matches_plain_path_every_step(asr, pdt, gdt, n, steps):
     """Race check for the bulk-copy pipeline: the same inputs updated through
     the pipelined kernel (16-byte-aligned buffers) and through the plain
-    kernel (the same data one element off alignment, which forces the scalar
-    path) with equal global indices must agree bit for bit after every step."""
+    kernel (the same data with params and grads one element and the moments
+    two elements off alignment: no element where all four buffers are
+    aligned, so no part of it can take the pipelined kernel) with equal
+    global indices must agree bit for bit after every step."""
     import torch
     gen = torch.Generator(device="cuda")
     gen.manual_seed(n + steps)
     pt = torch.bfloat16 if pdt == "bf16" else torch.float32
     gt = torch.bfloat16 if gdt == "bf16" else torch.float32
 
-    def pair(dtype, fill):
+    def pair(dtype, fill, shift):
         a = torch.empty(n, dtype=dtype, device="cuda")
         fill(a)
-        b_full = torch.empty(n + 1, dtype=dtype, device="cuda")
-        b = b_full[1:]
+        b_full = torch.empty(n + shift, dtype=dtype, device="cuda")
+        b = b_full[shift:]
         b.copy_(a)
         return a, b
 
-    pa, pb = pair(pt, lambda t: W.device_normal_(t, gen, 0.02))
-    ma, mb = pair(torch.float32, lambda t: W.device_normal_(t, gen, 1e-4))
-    va, vb = pair(torch.float32, lambda t: W.device_normal_(t, gen, 1e-6).abs_())
-    ga, gb = pair(gt, lambda t: W.device_normal_(t, gen, 1e-3))
+    pa, pb = pair(pt, lambda t: W.device_normal_(t, gen, 0.02), 1)
+    ma, mb = pair(torch.float32, lambda t: W.device_normal_(t, gen, 1e-4), 2)
+    va, vb = pair(torch.float32, lambda t: W.device_normal_(t, gen, 1e-6).abs_(), 2)
+    ga, gb = pair(gt, lambda t: W.device_normal_(t, gen, 1e-3), 1)
     assert pa.data_ptr() % 16 == 0 and pb.data_ptr() % 16 != 0
+    # no h < 8 puts all four of the shifted buffers on a 16-byte boundary
+    sizes = [pb.element_size(), gb.element_size(), 4, 4]
+    assert not any(all((t.data_ptr() + h * sz) % 16 == 0 for t, sz in zip((pb, gb, mb, vb), sizes))
+                   for h in range(8))
     asr.asr_take_device_error()
     for step in range(1, steps + 1):
         W.device_normal_(ga, gen, 1e-3)
