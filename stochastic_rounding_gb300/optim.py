@@ -55,8 +55,9 @@ class AdamWSR(torch.optim.Optimizer):
     ``rounding`` (``"sr"``, or ``"rne"`` for round-to-nearest-even, the
     biased baseline), ``base_offset`` (global position of the first
     parameter's element 0) and ``check_errors`` (when to read the device
-    error bit: ``True``, ``"deferred"`` or ``False``, see the module notes).  Parameters must be contiguous CUDA tensors of float32
-    or bfloat16; gradients dense float32 or bfloat16.
+    error bit: ``True``, ``"deferred"`` or ``False``; see the module notes).
+    Parameters must be contiguous CUDA tensors of float32 or bfloat16;
+    gradients dense float32 or bfloat16.
     """
 
     def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
