@@ -92,16 +92,21 @@ def traffic_per_param():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """nvidia-smi clock/throttle samples (every 50 ms, time-stamped) around the
+    timed region; `mark_start`/`mark_end` bracket the region on the host clock,
+    and `summary` keeps the samples taken inside it (the nearest one if the
+    region is shorter than the sampling period)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -109,12 +114,18 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -124,32 +135,54 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
-        if self.proc is None or not self.path:
-            return None
+    @staticmethod
+    def parse(lines):
+        """Rows of the CSV lines nvidia-smi wrote (malformed lines skipped)."""
+        import datetime
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
-                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
-                except ValueError:
-                    continue
-        os.remove(self.path)
+        for line in lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append(dict(t=ts, sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0=None, t1=None):
+        """Median SM clock, max clock, active slowdown reasons and peak power
+        over the rows taken within [t0, t1] (all rows without a window; the
+        row nearest the window's middle if none falls inside it)."""
         if not rows:
             return None
+        inside = rows
+        if t0 is not None and t1 is not None:
+            inside = [r for r in rows if t0 <= r["t"] <= t1]
+            if not inside:
+                mid = 0.5 * (t0 + t1)
+                inside = [min(rows, key=lambda r: abs(r["t"] - mid))]
         reasons = set()
-        for r in rows:
+        for r in inside:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
                               ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
                 if r[key].lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
-                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
-                "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["smax"] for r in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "period_ms": ClockSampler.PERIOD_MS,
+                "power_w_max": max(r["power"] for r in inside)}
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        with open(self.path) as f:
+            rows = self.parse(f)
+        os.remove(self.path)
+        return self.summarize(rows, self.t0, self.t1)
 
 
 def cpu_oracle_sample(steps, sample_elems=CPU_SAMPLE_ELEMS, seed=0):
@@ -549,6 +582,7 @@ def run_gpu(args):
     with ClockSampler(local) as clocks:
         all_start = torch.cuda.Event(enable_timing=True)
         all_end = torch.cuda.Event(enable_timing=True)
+        clocks.mark_start()
         all_start.record(stream)
         for k in range(args.steps):
             t_global += 1
@@ -557,6 +591,7 @@ def run_gpu(args):
             ends[k].record(stream)
         all_end.record(stream)
         torch.cuda.synchronize(dev)
+        clocks.mark_end()
     barrier()
     require_no_device_error(asr.asr_take_device_error, "timed device-resident steps")
     total_ms = max_over_ranks(all_start.elapsed_time(all_end))

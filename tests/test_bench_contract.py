@@ -56,3 +56,31 @@ def test_every_timed_region_is_checked_before_the_line_is_printed():
     regions = {r for _, r in checks}
     assert {"warm-up steps", "timed device-resident steps", "timed end-to-end steps"} <= regions
     assert prints and max(l for l, _ in checks) < min(prints)
+
+
+def test_clock_summary_keeps_the_samples_of_the_timed_region():
+    """The clock record covers the timed region only: samples outside the
+    host-clock window are dropped (an idle clock before the region must not
+    set the median), reasons are those seen inside it, and a region shorter
+    than the sampling period gets the sample nearest its middle."""
+    import datetime
+
+    import bench
+    base = datetime.datetime(2026, 1, 5, 10, 0, 0)
+
+    def line(ms, sm, reason="Not Active", pcap="Not Active"):
+        ts = (base + datetime.timedelta(milliseconds=ms)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return f"{ts}, 0, {sm}, 2070, 300.5, 0x0, {reason}, Not Active, Not Active, {pcap}"
+
+    lines = [line(0, 990), line(50, 990, reason="Active"), line(100, 2070), line(150, 2055, pcap="Active"),
+             line(200, 2070), line(250, 1200), "garbage", ""]
+    rows = bench.ClockSampler.parse(lines)
+    assert len(rows) == 6
+    t = lambda ms: (base + datetime.timedelta(milliseconds=ms)).timestamp()
+    s = bench.ClockSampler.summarize(rows, t(90), t(210))
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    one = bench.ClockSampler.summarize(rows, t(40), t(45))
+    assert one["samples"] == 1 and one["reasons"] == ["hw_slowdown"] and one["sm_mhz"] == 990
+    assert bench.ClockSampler.summarize(rows)["samples"] == 6
+    assert bench.ClockSampler.summarize([], t(0), t(1)) is None

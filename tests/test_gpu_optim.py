@@ -178,7 +178,7 @@ def _regression(asr, rounding, steps=1500, seed=0, orc=None, oracle_steps=0):
     hv = np.zeros(d * o, np.float32)
     hist = []
     for k in range(steps):
-        r = X @ W.float() - y
+        r = X @ W.detach().float() - y
         hist.append(float((r * r).mean()))
         W.grad = ((2.0 / n) * (X.t() @ r)).to(torch.bfloat16)
         opt.step()
