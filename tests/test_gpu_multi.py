@@ -109,6 +109,80 @@ def _check_windows(asr, orc, ps, table, windows, step, seed):
         assert_same_bits(host(ps.v[a:a + n]), v, f"{ps.table[t][0]}[{s}:{s + n}] v step {step}")
 
 
+def _host_view(t):
+    """A host copy of a device tensor as a numpy array (bf16 as uint16
+    patterns), without a second copy."""
+    import torch
+    a = t.detach().cpu()
+    if a.dtype == torch.bfloat16:
+        return a.view(torch.int16).numpy().view(np.uint16)
+    return a.numpy()
+
+
+def _mem_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+@pytest.mark.parametrize("shape,steps", [(W.LLAMA_1B, (1, 2)), (W.LLAMA_8B, (1,))],
+                         ids=["llama-1.5B-147t", "llama3-8B-291t"])
+def test_llama_param_set_every_element(asr, orc, shape, steps):
+    """Every element of every tensor of a Llama-shaped set, after one
+    multi-tensor launch per step, equals the oracle run at the tensor's base
+    index (host threads, each on a contiguous chunk; the oracle call releases
+    the interpreter lock).  Moments start from nonzero values so each term of
+    the update is exercised from the first step.  Skipped where the host lacks
+    the memory for one host copy of the set."""
+    import concurrent.futures
+    import os
+
+    import torch
+    from stochastic_rounding_gb300 import _lib
+    table = W.param_table(shape)
+    _, total = W.offsets(table)
+    need = total * 12 + max(n for _, n, _ in table) * 10
+    if _mem_available() < need * 1.25 + (8 << 30):
+        pytest.skip(f"host memory: {need / 2**30:.0f} GiB for one copy of the set")
+    ps = W.DeviceParamSet(shape, seed=5)
+    W.device_normal_(ps.m, ps.gen, 1e-4)
+    W.device_normal_(ps.v, ps.gen, 1e-6)
+    ps.v.abs_()
+    dev_table = _lib.make_table(ps.tensors())
+    workers = max(1, len(os.sched_getaffinity(0)))
+    chunk = 1 << 24
+    jobs = [(s + a, min(s + n, s + a + chunk)) for s, n in zip(ps.starts, ps.sizes) for a in range(0, n, chunk)]
+    with concurrent.futures.ThreadPoolExecutor(workers) as pool:
+        for k, step in enumerate(steps):
+            if k > 0:
+                ps.new_grads()
+            torch.cuda.synchronize()
+            p, g, m, v = (_host_view(x) for x in (ps.p, ps.g, ps.m, ps.v))
+            asr.asr_adamw_sr_multi_tensor(dev_table, step=step, seed=0, device=ps.device, **HP)
+
+            def run(lo_hi, step=step):
+                lo, hi = lo_hi
+                orc.adamw_step(p[lo:hi], g[lo:hi], m[lo:hi], v[lo:hi], step=step, seed=0, base_index=lo, **HP)
+
+            list(pool.map(run, jobs))
+            torch.cuda.synchronize()
+            for (name, n, _), s in zip(ps.table, ps.starts):
+                for got, want, what in ((ps.p, p, "p"), (ps.m, m, "m"), (ps.v, v, "v")):
+                    gh = _host_view(got[s:s + n])
+                    w = want[s:s + n]
+                    u = np.uint16 if w.dtype == np.uint16 else np.uint32
+                    if not np.array_equal(gh.view(u), w.view(u)):
+                        assert_same_bits(gh, w, f"{name} {what} step {step}")
+            del p, g, m, v
+    del ps, dev_table
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("shape,steps,checked", [(W.LLAMA_1B, 20, (1, 2, 20)), (W.LLAMA_8B, 10, (1, 10))],
                          ids=["llama-1.5B-147t-20steps", "llama3-8B-291t-10steps"])
 def test_llama_param_set_sampled(asr, orc, shape, steps, checked):
