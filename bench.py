@@ -145,22 +145,31 @@ class ClockSampler:
             if len(parts) < 10:
                 continue
             try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append(dict(t=ts, sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
-                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+                row = dict(sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                           hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9])
             except ValueError:
                 continue
+            row["t"] = None
+            for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+                try:
+                    row["t"] = datetime.datetime.strptime(parts[0], fmt).timestamp()
+                    break
+                except ValueError:
+                    pass
+            rows.append(row)
         return rows
 
     @staticmethod
     def summarize(rows, t0=None, t1=None):
         """Median SM clock, max clock, active slowdown reasons and peak power
-        over the rows taken within [t0, t1] (all rows without a window; the
-        row nearest the window's middle if none falls inside it)."""
+        over the rows taken within [t0, t1] (all rows without a window or
+        with an unreadable timestamp; the row nearest the window's middle if
+        none falls inside it)."""
         if not rows:
             return None
-        inside = rows
-        if t0 is not None and t1 is not None:
+        inside, window = rows, "all samples"
+        if t0 is not None and t1 is not None and all(r["t"] is not None for r in rows):
+            window = "timed region"
             inside = [r for r in rows if t0 <= r["t"] <= t1]
             if not inside:
                 mid = 0.5 * (t0 + t1)
@@ -173,7 +182,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(r["sm"] for r in inside),
                 "sm_max_mhz": max(r["smax"] for r in inside), "reasons": sorted(reasons),
-                "samples": len(inside), "period_ms": ClockSampler.PERIOD_MS,
+                "samples": len(inside), "period_ms": ClockSampler.PERIOD_MS, "window": window,
                 "power_w_max": max(r["power"] for r in inside)}
 
     def summary(self):

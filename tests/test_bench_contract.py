@@ -82,5 +82,10 @@ def test_clock_summary_keeps_the_samples_of_the_timed_region():
     assert s["reasons"] == ["sw_power_cap"]
     one = bench.ClockSampler.summarize(rows, t(40), t(45))
     assert one["samples"] == 1 and one["reasons"] == ["hw_slowdown"] and one["sm_mhz"] == 990
+    assert s["window"] == "timed region"
     assert bench.ClockSampler.summarize(rows)["samples"] == 6
+    odd = bench.ClockSampler.parse(["12:00:01 PM, 0, 1980, 2070, 300.5, 0x0, Not Active, Not Active, "
+                                    "Not Active, Not Active"])
+    s = bench.ClockSampler.summarize(rows + odd, t(90), t(210))
+    assert s["samples"] == 7 and s["window"] == "all samples"
     assert bench.ClockSampler.summarize([], t(0), t(1)) is None

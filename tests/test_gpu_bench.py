@@ -2,7 +2,8 @@
 layout (the leading tensors, ~20M params; the other configurations are left
 out at such sizes): one JSON line with the contract's keys, a positive
 throughput, the roofline fraction of a kernel that does its work, the e2e
-leg with its link rates and copies-only pipeline, and no device error."""
+leg with its link rates and copies-only pipeline, clock samples taken within
+the timed region (where nvidia-smi runs), and no device error."""
 import json
 import os
 import subprocess
@@ -38,3 +39,5 @@ def test_bench_native_arm_small():
     assert e2e["copies_only_gparams_s"] > 0 and set(e2e["link_gbs"]) == {"h2d", "d2h", "both"}
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["all_cores"]["cores"] >= 1
+    clk = d["clocks"]
+    assert clk is None or (clk["window"] == "timed region" and clk["samples"] >= 1 and clk["sm_mhz"] > 0), clk
