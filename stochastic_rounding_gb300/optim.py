@@ -177,6 +177,12 @@ class AdamWSR(torch.optim.Optimizer):
         if closure is not None:
             with torch.enable_grad():
                 loss = closure()
+        # every parameter is checked before anything is launched or counted,
+        # so a refused parameter leaves the whole model as it was
+        for group in self.param_groups:
+            for p in group["params"]:
+                if p.grad is not None:
+                    self._check(p)
         devices = set()
         for group in self.param_groups:
             beta1, beta2 = group["betas"]
@@ -185,7 +191,6 @@ class AdamWSR(torch.optim.Optimizer):
             for p in group["params"]:
                 if p.grad is None:
                     continue
-                self._check(p)
                 state = self.state[p]
                 if len(state) == 0:
                     state["step"] = 0

@@ -100,3 +100,28 @@ def test_step_without_error_checks_reads_nothing(monkeypatch):
     fake.bits = 0
     opt.step(check_errors=True)               # clean word: no exception
     assert fake.reads == 1
+
+
+def test_a_refused_parameter_leaves_every_group_unstepped(monkeypatch):
+    """A parameter the optimizer refuses in the second group raises before
+    the first group is launched, and no step count moves."""
+    from stochastic_rounding_gb300 import optim
+    fake = _FakeLib(0)
+    refused = set()
+
+    def check(p):
+        if id(p) in refused:
+            raise ValueError("refused parameter")
+
+    monkeypatch.setattr(optim, "_lib", fake)
+    monkeypatch.setattr(AdamWSR, "_check", staticmethod(check))
+    a, b = torch.nn.Parameter(torch.zeros(4)), torch.nn.Parameter(torch.zeros(6))
+    a.grad, b.grad = torch.zeros(4), torch.zeros(6)
+    opt = AdamWSR([{"params": [a]}, {"params": [b]}])
+    refused.add(id(b))
+    with pytest.raises(ValueError, match="refused"):
+        opt.step()
+    assert fake.calls == [] and len(opt.state) == 0
+    refused.clear()
+    opt.step()
+    assert [s for _, s in fake.calls] == [1, 1] and opt.state[a]["step"] == 1
