@@ -169,12 +169,18 @@ def _torch():
     return torch
 
 
-def _dev_ptr(t, name, dtypes, numel=None):
+def _dev_ptr(t, name, dtypes, numel=None, device=None):
+    """Device pointer of ``t`` after the checks the C ABI cannot make: a
+    contiguous CUDA tensor of one of ``dtypes`` (and ``numel`` elements),
+    on ``device`` when given -- a kernel runs on one device, and a pointer
+    into another device's memory would be dereferenced there."""
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}; the call's other tensors are on {device}")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
     if not t.is_contiguous():
@@ -243,11 +249,11 @@ def asr_stochastic_round_bf16(x, out, *, base_index: int = 0, step: int = 0, see
     torch = _torch()
     n = x.numel()
     px = _dev_ptr(x, "x", (torch.float32,))
-    po = _dev_ptr(out, "out", (torch.bfloat16, torch.int16), n)
+    po = _dev_ptr(out, "out", (torch.bfloat16, torch.int16), n, x.device)
     pr = None
     if rbits is not None:
         dts = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
-        pr = _dev_ptr(rbits, "rbits", dts, n)
+        pr = _dev_ptr(rbits, "rbits", dts, n, x.device)
     with _on_device(x.device):
         _check(lib().asr_stochastic_round_bf16(px, pr, po, n, int(base_index), int(step) & 0xFFFFFFFF,
                                                int(seed) & (2**64 - 1), _stream_handle(x.device, stream)),
@@ -269,27 +275,32 @@ def asr_adamw_sr_step(param, grad, exp_avg, exp_avg_sq, *, lr, beta1=0.9, beta2=
     torch = _torch()
     n = param.numel()
     pp = _dev_ptr(param, "param", (torch.float32, torch.bfloat16, torch.int16))
-    pg = _dev_ptr(grad, "grad", (torch.float32, torch.bfloat16, torch.int16), n)
-    pm = _dev_ptr(exp_avg, "exp_avg", (torch.float32,), n)
-    pv = _dev_ptr(exp_avg_sq, "exp_avg_sq", (torch.float32,), n)
+    dev = param.device
+    pg = _dev_ptr(grad, "grad", (torch.float32, torch.bfloat16, torch.int16), n, dev)
+    pm = _dev_ptr(exp_avg, "exp_avg", (torch.float32,), n, dev)
+    pv = _dev_ptr(exp_avg_sq, "exp_avg_sq", (torch.float32,), n, dev)
     h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
-    with _on_device(param.device):
+    with _on_device(dev):
         _check(lib().asr_adamw_sr_step(pp, _dt(param), pg, _dt(grad), pm, pv, n, int(base_index),
-                                       ctypes.byref(h), _stream_handle(param.device, stream)),
+                                       ctypes.byref(h), _stream_handle(dev, stream)),
                "asr_adamw_sr_step")
 
 
 def make_table(tensors: Sequence[Sequence]) -> ctypes.Array:
-    """Descriptor array from (param, grad, exp_avg, exp_avg_sq, base_index) tuples."""
+    """Descriptor array from (param, grad, exp_avg, exp_avg_sq, base_index)
+    tuples, all on one CUDA device (the first parameter's)."""
     torch = _torch()
     arr = (TensorDesc * len(tensors))()
+    dev = None
     for i, (p, g, m, v, base) in enumerate(tensors):
         n = p.numel()
+        pp = _dev_ptr(p, f"param[{i}]", (torch.float32, torch.bfloat16, torch.int16), None, dev)
+        dev = p.device
         arr[i] = TensorDesc(
-            _dev_ptr(p, f"param[{i}]", (torch.float32, torch.bfloat16, torch.int16)),
-            _dev_ptr(g, f"grad[{i}]", (torch.float32, torch.bfloat16, torch.int16), n),
-            _dev_ptr(m, f"exp_avg[{i}]", (torch.float32,), n),
-            _dev_ptr(v, f"exp_avg_sq[{i}]", (torch.float32,), n),
+            pp,
+            _dev_ptr(g, f"grad[{i}]", (torch.float32, torch.bfloat16, torch.int16), n, dev),
+            _dev_ptr(m, f"exp_avg[{i}]", (torch.float32,), n, dev),
+            _dev_ptr(v, f"exp_avg_sq[{i}]", (torch.float32,), n, dev),
             n, int(base), _dt(p), _dt(g))
     return arr
 
@@ -346,10 +357,12 @@ def asr_gemm_bf16_sr(a, b, c, c_f32=None, *, rounding="sr", step=0, seed=0, stre
     if b.shape[1] != k or tuple(c.shape) != (m, n):
         raise ValueError(f"shapes do not chain: a {tuple(a.shape)}, b {tuple(b.shape)}, c {tuple(c.shape)}")
     pa = _dev_ptr(a, "a", (torch.bfloat16,))
-    pb = _dev_ptr(b, "b", (torch.bfloat16,))
-    pc = _dev_ptr(c, "c", (torch.bfloat16,))
-    pf = _dev_ptr(c_f32, "c_f32", (torch.float32,), m * n) if c_f32 is not None else None
-    r = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE}[rounding]
+    pb = _dev_ptr(b, "b", (torch.bfloat16,), None, a.device)
+    pc = _dev_ptr(c, "c", (torch.bfloat16,), None, a.device)
+    pf = _dev_ptr(c_f32, "c_f32", (torch.float32,), m * n, a.device) if c_f32 is not None else None
+    r = _ROUNDING.get(rounding)
+    if r is None:
+        raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")
     with _on_device(a.device):
         _check(lib().asr_gemm_bf16_sr(pa, pb, pc, pf, m, n, k, r, int(step) & 0xFFFFFFFF,
                                       int(seed) & (2**64 - 1), _stream_handle(a.device, stream)),

@@ -68,3 +68,47 @@ def test_package_exports_both_wrappers():
     import stochastic_rounding_gb300 as asr
     for name in NAMES:
         assert getattr(asr, name) is getattr(_lib, name)
+
+
+class _OnDevice(__import__("torch").Tensor):
+    """A CPU tensor that reports itself as living on cuda:<idx>, so the
+    binding's device checks can be exercised without a GPU (no pointer of
+    it ever reaches the library here)."""
+
+    @property
+    def is_cuda(self):
+        return True
+
+    @property
+    def device(self):
+        import torch
+        return torch.device("cuda", self._idx)
+
+
+def _on(idx, *shape, dtype=None):
+    import torch
+    t = torch.Tensor._make_subclass(_OnDevice, torch.zeros(*shape, dtype=dtype or torch.float32))
+    t._idx = idx
+    return t
+
+
+def test_tensors_on_another_device_are_refused_before_any_call(stub):
+    """A kernel runs on one device: a grad, moment, output or operand on
+    another device is refused by the binding instead of being handed to the
+    kernel as a foreign pointer."""
+    import torch
+    fake = stub(_lib.ASR_OK)
+    p, g, m, v = _on(0, 8, dtype=torch.bfloat16), _on(0, 8, dtype=torch.bfloat16), _on(0, 8), _on(0, 8)
+    _lib.make_table([(p, g, m, v, 0)])                       # one device: accepted
+    with pytest.raises(ValueError, match="cuda:1"):
+        _lib.make_table([(p, g, m, v, 0), (_on(1, 8), _on(1, 8), _on(1, 8), _on(1, 8), 8)])
+    with pytest.raises(ValueError, match="exp_avg_sq"):
+        _lib.make_table([(p, g, m, _on(1, 8), 0)])
+    with pytest.raises(ValueError, match="grad"):
+        _lib.asr_adamw_sr_step(p, _on(1, 8, dtype=torch.bfloat16), m, v, lr=1e-3, step=1)
+    with pytest.raises(ValueError, match="out"):
+        _lib.asr_stochastic_round_bf16(_on(0, 8), _on(1, 8, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="b is on"):
+        _lib.asr_gemm_bf16_sr(_on(0, 4, 8, dtype=torch.bfloat16), _on(1, 4, 8, dtype=torch.bfloat16),
+                              _on(0, 4, 4, dtype=torch.bfloat16))
+    assert sum(fake.calls.values()) == 0
