@@ -15,6 +15,9 @@
  * Conventions shared by every entry point
  *   - Buffer pointers are DEVICE pointers (anything a kernel can dereference:
  *     cudaMalloc / torch CUDA memory, managed memory), owned by the caller.
+ *     The kernels run on the calling thread's current device, so every
+ *     buffer of a call must be memory that device can reach (its own, or a
+ *     peer's with peer access enabled); the library cannot check this.
  *     The library allocates no memory at run time.  What it keeps between
  *     calls: per-device caches of launch shapes (and the tensor-map encoder's
  *     address), a 4-byte device error word with a 4-byte copy slot
