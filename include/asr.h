@@ -18,10 +18,14 @@
  *     The kernels run on the calling thread's current device, so every
  *     buffer of a call must be memory that device can reach (its own, or a
  *     peer's with peer access enabled); the library cannot check this.
- *     The library allocates no memory at run time.  What it keeps between
+ *     The library allocates no device memory at run time (host scratch:
+ *     asr_adamw_sr_multi_tensor may take a host buffer of two descriptors
+ *     per tensor for the duration of the call; the static variant below
+ *     takes none).  What it keeps between
  *     calls: per-device caches of launch shapes (and the tensor-map encoder's
- *     address), a 4-byte device error word with a 4-byte copy slot
- *     (asr_take_device_error) and the static descriptor array of
+ *     address), a 4-byte device error word with 64 four-byte copy slots
+ *     (one per asr_take_device_error in progress) and the static
+ *     descriptor array of
  *     asr_adamw_sr_multi_tensor_static.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising the host.  Buffers

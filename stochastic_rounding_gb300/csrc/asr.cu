@@ -38,6 +38,7 @@
 #include <cstring>
 #include <memory>
 #include <mutex>
+#include <thread>
 #include <unordered_map>
 
 #include "asr.h"
@@ -52,18 +53,50 @@ namespace {
 // Takes the device error bits: reads and clears the word in one atomic step
 // (so no bit set by a kernel still running elsewhere is lost between the two)
 // and writes them to dst -- device memory, or page-locked host memory that
-// the GPU can write -- or, with dst null, to g_error_taken.
-__device__ unsigned int g_error_taken = 0;
+// the GPU can write -- or, with dst null, to copy slot `slot` of
+// g_error_taken, from which the blocking take copies them to the host.  Each
+// blocking take in progress holds its own slot, so concurrent takes from
+// several host threads cannot read one another's bits.
+constexpr int kTakeSlots = 64;
+__device__ unsigned int g_error_taken[kTakeSlots];
 
-__global__ void take_error_kernel(unsigned int *dst)
+__global__ void take_error_kernel(unsigned int *dst, int slot)
 {
     const unsigned int bits = atomicExch(&g_device_error, 0u);
-    *(dst ? dst : &g_error_taken) = bits;
+    *(dst ? dst : &g_error_taken[slot]) = bits;
 }
 
 // ------------------------------------------------------------- host side
 
 thread_local int g_last_cuda_error = 0;
+
+// Copy slots of the blocking error take: a slot is held from its launch to
+// the end of its host copy.  With every slot in use (kTakeSlots takes in
+// progress at once) the caller yields until one is released.
+std::mutex g_take_mu;
+uint64_t g_take_busy = 0;
+static_assert(kTakeSlots == 64, "one bit of g_take_busy per slot");
+
+int take_slot()
+{
+    for (;;) {
+        {
+            std::lock_guard<std::mutex> lk(g_take_mu);
+            if (~g_take_busy) {
+                const int slot = __builtin_ctzll(~g_take_busy);
+                g_take_busy |= 1ull << slot;
+                return slot;
+            }
+        }
+        std::this_thread::yield();
+    }
+}
+
+void release_slot(int slot)
+{
+    std::lock_guard<std::mutex> lk(g_take_mu);
+    g_take_busy &= ~(1ull << slot);
+}
 
 asr_status cuda_fail(cudaError_t e)
 {
@@ -441,11 +474,14 @@ asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream)
 {
     if (!bits) return ASR_ERR_INVALID_VALUE;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    take_error_kernel<<<1, 1, 0, s>>>(nullptr);
+    const int slot = take_slot();
+    take_error_kernel<<<1, 1, 0, s>>>(nullptr, slot);
     cudaError_t e = cudaGetLastError();
     unsigned int h = 0;
-    if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(&h, g_error_taken, sizeof(h), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbolAsync(&h, g_error_taken, sizeof(h), sizeof(h) * slot, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    release_slot(slot);
     if (e != cudaSuccess) return cuda_fail(e);
     *bits = h;
     return ASR_OK;
@@ -467,7 +503,7 @@ asr_status asr_take_device_error_async(uint32_t *bits, asr_stream_t stream)
     if (e != cudaSuccess) return cuda_fail(e);
     if (a.type == cudaMemoryTypeDevice && a.device != dev) return ASR_ERR_INVALID_VALUE;
     take_error_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<unsigned int *>(a.devicePointer));
+        static_cast<unsigned int *>(a.devicePointer), 0);
     return check_launch();
 }
 

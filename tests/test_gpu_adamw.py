@@ -333,6 +333,50 @@ def test_bounded_wait_gives_up_with_a_status(asr):
     assert asr.asr_take_device_error() == 0
 
 
+def test_concurrent_blocking_takes_see_each_bit_once(asr):
+    """Blocking takes from several host threads at once, each on its own
+    stream: after one raised bit, exactly one of the takes of a round reports
+    it and the others report 0 -- none reads another call's copy of the
+    word.  Two hundred rounds of four threads released together."""
+    import threading
+
+    import torch
+    asr.asr_take_device_error()
+    threads_n, rounds = 4, 200
+    streams = [torch.cuda.Stream() for _ in range(threads_n)]
+    barrier = threading.Barrier(threads_n + 1)
+    results = [[0] * rounds for _ in range(threads_n)]
+    failures = []
+
+    def worker(i):
+        try:
+            for r in range(rounds):
+                barrier.wait()
+                results[i][r] = asr.asr_take_device_error(stream=streams[i])
+                barrier.wait()
+        except Exception as exc:          # reported by the main thread
+            failures.append(exc)
+            barrier.abort()
+
+    workers = [threading.Thread(target=worker, args=(i,)) for i in range(threads_n)]
+    for w in workers:
+        w.start()
+    try:
+        for r in range(rounds):
+            asr.asr_selftest_wait_timeout(20_000)
+            torch.cuda.synchronize()
+            barrier.wait()
+            barrier.wait()
+    finally:
+        for w in workers:
+            w.join(timeout=60)
+    assert not failures, failures
+    for r in range(rounds):
+        got = [results[i][r] for i in range(threads_n)]
+        assert sorted(got) == [0] * (threads_n - 1) + [1], (r, got)
+    assert asr.asr_take_device_error() == 0
+
+
 def test_error_bits_taken_without_waiting(asr):
     """asr_take_device_error_async: after a wait that gave up (the self-test)
     the bits land in page-locked host memory, or in device memory, once the
