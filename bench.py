@@ -274,6 +274,49 @@ def host_link_rates(dev, nbytes=1 << 30, reps=3):
     return rates
 
 
+def ring_copies_seconds(g_dev, p_dev, n, dev, steps, chunk=1 << 26, slots=2):
+    """Seconds per step of the end-to-end leg's transfers alone (2 B per param in,
+    2 B out, contiguous chunk-element ranges, host-to-device on one stream and
+    device-to-host of each range after its own host-to-device on another)
+    through a small ring of page-locked staging buffers -- ``slots`` per
+    direction, 512 MB in all by default -- instead of host buffers for the
+    whole set.  Measured outside the timed steps, after one untimed pass: on
+    hosts whose page-locked transfers stall in proportion to the page-locked
+    footprint it shows what the link gives the same bytes without that."""
+    import torch
+    g_ring = [torch.empty(chunk, dtype=g_dev.dtype, pin_memory=True) for _ in range(slots)]
+    p_ring = [torch.empty(chunk, dtype=p_dev.dtype, pin_memory=True) for _ in range(slots)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    main = torch.cuda.current_stream(dev)
+    ranges = [(lo, min(n, lo + chunk)) for lo in range(0, n, chunk)]
+
+    def one_pass():
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        for c, (lo, hi) in enumerate(ranges):
+            with torch.cuda.stream(s_in):
+                g_dev[lo:hi].copy_(g_ring[c % slots][:hi - lo], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev)
+                p_ring[c % slots][:hi - lo].copy_(p_dev[lo:hi], non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    one_pass()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for _ in range(steps):
+        one_pass()
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    seconds = e0.elapsed_time(e1) / 1e3 / steps
+    del g_ring, p_ring
+    return seconds
+
+
 def e2e_chunks(tensors, offset, max_params=1 << 28):
     """Consecutive tensors grouped into chunks of at most max_params (a larger
     tensor is a chunk of its own).  Each chunk is a contiguous range [lo, hi)
@@ -691,6 +734,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     copies_value = world * n * e_steps / (max_over_ranks(c_start.elapsed_time(c_end)) / 1e3) / 1e9
     del g_host, p_host
+    ring_value = world * n / max_over_ranks(ring_copies_seconds(ps.g, ps.p, n, dev, e_steps)) / 1e9
     link = host_link_rates(dev)
     # the copies alone bound the end-to-end step: 2n bytes in and 2n out
     floor_s = max(2 * n / (link["h2d"] * 1e9), 2 * n / (link["d2h"] * 1e9), 4 * n / (link["both"] * 1e9))
@@ -727,8 +771,12 @@ def run_gpu(args):
                     "link_gbs": link, "link_floor_gparams_s": n / floor_s / 1e9,
                     "frac_of_link_floor": e2e_value / world / (n / floor_s / 1e9),
                     "copies_only_gparams_s": copies_value, "frac_of_copies_only": e2e_value / copies_value,
+                    "small_footprint_copies_gparams_s": ring_value,
                     "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host; "
-                            "chunks of consecutive tensors pipelined over three streams"},
+                            "chunks of consecutive tensors pipelined over three streams; host buffers "
+                            "hold the whole set (copies_only: the same pipeline without the step calls; "
+                            "small_footprint_copies: the same bytes through a 512 MB page-locked "
+                            "staging ring, no step calls)"},
             "gpu_launches": launches,
             "configs": others,
             "clocks": clock,

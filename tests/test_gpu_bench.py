@@ -37,6 +37,7 @@ def test_bench_native_arm_small():
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] == 2 * d["config"]["params_per_gpu"]
     assert e2e["copies_only_gparams_s"] > 0 and set(e2e["link_gbs"]) == {"h2d", "d2h", "both"}
+    assert e2e["small_footprint_copies_gparams_s"] > 0
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["all_cores"]["cores"] >= 1
     clk = d["clocks"]
