@@ -89,3 +89,24 @@ def test_clock_summary_keeps_the_samples_of_the_timed_region():
     s = bench.ClockSampler.summarize(rows + odd, t(90), t(210))
     assert s["samples"] == 7 and s["window"] == "all samples"
     assert bench.ClockSampler.summarize([], t(0), t(1)) is None
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    """Launched the way multi-GPU runs are (torchrun, two ranks, loopback
+    rendezvous), the reference arm prints exactly one JSON line -- rank 0's,
+    with n_gpus = 2 -- and every rank exits 0."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["config"]["params_per_gpu"] == 8_030_261_248
