@@ -11,6 +11,7 @@ from __future__ import annotations
 import contextlib
 import ctypes
 import os
+import struct
 from typing import Optional, Sequence
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -154,12 +155,22 @@ def _check(status: int, what: str):
 _ROUNDING = {"sr": ASR_ROUND_SR, "rne": ASR_ROUND_RNE, ASR_ROUND_SR: ASR_ROUND_SR, ASR_ROUND_RNE: ASR_ROUND_RNE}
 
 
+# AdamwHparams packed in one call (its fields in order, native alignment):
+# one struct.pack is a fraction of the cost of eight ctypes field stores.
+_HP_PACK = struct.Struct("=5dIIQ")
+assert _HP_PACK.size == ctypes.sizeof(AdamwHparams)
+
+
 def make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding="sr") -> AdamwHparams:
     r = _ROUNDING.get(rounding)
     if r is None:
         raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")
-    return AdamwHparams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
-                        int(step), r, int(seed) & (2**64 - 1))
+    h = AdamwHparams()
+    try:
+        _HP_PACK.pack_into(h, 0, lr, beta1, beta2, eps, weight_decay, step, r, int(seed) & (2**64 - 1))
+    except struct.error as exc:
+        raise ValueError(f"hyperparameters out of range (step must fit in 32 bits): {exc}") from None
+    return h
 
 
 # ------------------------------------------------------------ tensor helpers
@@ -172,15 +183,16 @@ def _torch():
 def _dev_ptr(t, name, dtypes, numel=None, device=None):
     """Device pointer of ``t`` after the checks the C ABI cannot make: a
     contiguous CUDA tensor of one of ``dtypes`` (and ``numel`` elements),
-    on ``device`` when given -- a kernel runs on one device, and a pointer
-    into another device's memory would be dereferenced there."""
+    on CUDA device index ``device`` when given -- a kernel runs on one
+    device, and a pointer into another device's memory would be
+    dereferenced there."""
     torch = _torch()
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
-    if device is not None and t.device != device:
-        raise ValueError(f"{name} is on {t.device}; the call's other tensors are on {device}")
+    if device is not None and t.get_device() != device:
+        raise ValueError(f"{name} is on cuda:{t.get_device()}; the call's other tensors are on cuda:{device}")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
     if not t.is_contiguous():
@@ -218,13 +230,17 @@ def _stream_handle(device, stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+_DTYPES = {}
+
+
 def _dt(t):
-    torch = _torch()
-    if t.dtype == torch.float32:
-        return ASR_F32
-    if t.dtype in (torch.bfloat16, torch.int16):
-        return ASR_BF16
-    raise TypeError(f"unsupported dtype {t.dtype}")
+    if not _DTYPES:
+        torch = _torch()
+        _DTYPES.update({torch.float32: ASR_F32, torch.bfloat16: ASR_BF16, torch.int16: ASR_BF16})
+    code = _DTYPES.get(t.dtype)
+    if code is None:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return code
 
 
 # ------------------------------------------------------------- entry points
@@ -249,11 +265,12 @@ def asr_stochastic_round_bf16(x, out, *, base_index: int = 0, step: int = 0, see
     torch = _torch()
     n = x.numel()
     px = _dev_ptr(x, "x", (torch.float32,))
-    po = _dev_ptr(out, "out", (torch.bfloat16, torch.int16), n, x.device)
+    xd = x.get_device()
+    po = _dev_ptr(out, "out", (torch.bfloat16, torch.int16), n, xd)
     pr = None
     if rbits is not None:
         dts = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
-        pr = _dev_ptr(rbits, "rbits", dts, n, x.device)
+        pr = _dev_ptr(rbits, "rbits", dts, n, xd)
     with _on_device(x.device):
         _check(lib().asr_stochastic_round_bf16(px, pr, po, n, int(base_index), int(step) & 0xFFFFFFFF,
                                                int(seed) & (2**64 - 1), _stream_handle(x.device, stream)),
@@ -276,9 +293,10 @@ def asr_adamw_sr_step(param, grad, exp_avg, exp_avg_sq, *, lr, beta1=0.9, beta2=
     n = param.numel()
     pp = _dev_ptr(param, "param", (torch.float32, torch.bfloat16, torch.int16))
     dev = param.device
-    pg = _dev_ptr(grad, "grad", (torch.float32, torch.bfloat16, torch.int16), n, dev)
-    pm = _dev_ptr(exp_avg, "exp_avg", (torch.float32,), n, dev)
-    pv = _dev_ptr(exp_avg_sq, "exp_avg_sq", (torch.float32,), n, dev)
+    di = param.get_device()
+    pg = _dev_ptr(grad, "grad", (torch.float32, torch.bfloat16, torch.int16), n, di)
+    pm = _dev_ptr(exp_avg, "exp_avg", (torch.float32,), n, di)
+    pv = _dev_ptr(exp_avg_sq, "exp_avg_sq", (torch.float32,), n, di)
     h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
     with _on_device(dev):
         _check(lib().asr_adamw_sr_step(pp, _dt(param), pg, _dt(grad), pm, pv, n, int(base_index),
@@ -295,7 +313,7 @@ def make_table(tensors: Sequence[Sequence]) -> ctypes.Array:
     for i, (p, g, m, v, base) in enumerate(tensors):
         n = p.numel()
         pp = _dev_ptr(p, f"param[{i}]", (torch.float32, torch.bfloat16, torch.int16), None, dev)
-        dev = p.device
+        dev = p.get_device()
         arr[i] = TensorDesc(
             pp,
             _dev_ptr(g, f"grad[{i}]", (torch.float32, torch.bfloat16, torch.int16), n, dev),
@@ -357,9 +375,10 @@ def asr_gemm_bf16_sr(a, b, c, c_f32=None, *, rounding="sr", step=0, seed=0, stre
     if b.shape[1] != k or tuple(c.shape) != (m, n):
         raise ValueError(f"shapes do not chain: a {tuple(a.shape)}, b {tuple(b.shape)}, c {tuple(c.shape)}")
     pa = _dev_ptr(a, "a", (torch.bfloat16,))
-    pb = _dev_ptr(b, "b", (torch.bfloat16,), None, a.device)
-    pc = _dev_ptr(c, "c", (torch.bfloat16,), None, a.device)
-    pf = _dev_ptr(c_f32, "c_f32", (torch.float32,), m * n, a.device) if c_f32 is not None else None
+    ad = a.get_device()
+    pb = _dev_ptr(b, "b", (torch.bfloat16,), None, ad)
+    pc = _dev_ptr(c, "c", (torch.bfloat16,), None, ad)
+    pf = _dev_ptr(c_f32, "c_f32", (torch.float32,), m * n, ad) if c_f32 is not None else None
     r = _ROUNDING.get(rounding)
     if r is None:
         raise ValueError(f"rounding must be 'sr' or 'rne', not {rounding!r}")

@@ -84,6 +84,9 @@ class _OnDevice(__import__("torch").Tensor):
         import torch
         return torch.device("cuda", self._idx)
 
+    def get_device(self):
+        return self._idx
+
 
 def _on(idx, *shape, dtype=None):
     import torch
