@@ -60,11 +60,33 @@ struct PhiloxParams {
     RoundKeys keys;
 };
 
+// Counters per thread and loop iteration in the aligned case, as independent
+// chains: a thread's Philox calls are ten dependent rounds of multiplies, so
+// two calls in flight per thread keep the integer-multiply pipe busier (the
+// op is bound by that pipe and by its 16-byte stores).
+#ifndef ASR_PHILOX_CHAINS
+#define ASR_PHILOX_CHAINS 3
+#endif
+constexpr int kPhiloxChains = ASR_PHILOX_CHAINS;
+
 template <bool ALIGNED16>
 __global__ void __launch_bounds__(kThreads) philox_kernel(const __grid_constant__ PhiloxParams P)
 {
-    for (uint64_t j = blockIdx.x * static_cast<uint64_t>(kThreads) + threadIdx.x; j < P.n_ctr;
-         j += static_cast<uint64_t>(gridDim.x) * kThreads) {
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kThreads;
+    uint64_t j = blockIdx.x * static_cast<uint64_t>(kThreads) + threadIdx.x;
+    // kPhiloxChains counters j, j + stride, ... per iteration while all are in range
+    for (; ALIGNED16 && j + (kPhiloxChains - 1) * stride < P.n_ctr; j += kPhiloxChains * stride) {
+        uint32_t w[kPhiloxChains][4];
+#pragma unroll
+        for (int q = 0; q < kPhiloxChains; ++q) {
+            const uint64_t c = P.ctr_base + j + q * stride;
+            philox4x32_10(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), P.ctr2, P.ctr3, P.keys, w[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < kPhiloxChains; ++q)
+            st_stream(P.out + 4 * (j + q * stride), make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]));
+    }
+    for (; j < P.n_ctr; j += stride) {
         const uint64_t c = P.ctr_base + j;
         uint32_t w[4];
         philox4x32_10(static_cast<uint32_t>(c), static_cast<uint32_t>(c >> 32), P.ctr2, P.ctr3, P.keys, w);
