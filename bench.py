@@ -631,6 +631,7 @@ def run_gpu(args):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize(dev)
+    counts_before = asr.asr_kernel_launches()
     with ClockSampler(local) as clocks:
         all_start = torch.cuda.Event(enable_timing=True)
         all_end = torch.cuda.Event(enable_timing=True)
@@ -644,13 +645,17 @@ def run_gpu(args):
         all_end.record(stream)
         torch.cuda.synchronize(dev)
         clocks.mark_end()
+    counts_after = asr.asr_kernel_launches()
     barrier()
     require_no_device_error(asr.asr_take_device_error, "timed device-resident steps")
     total_ms = max_over_ranks(all_start.elapsed_time(all_end))
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     launch_ms = statistics.mean(per_launch_ms)
     clock = clocks.summary()
-    launches = args.steps * 1                       # one multi-tensor launch per step
+    # the library's own launch counters over the timed region (one
+    # multi-tensor launch per step expected)
+    launches = sum(counts_after[k] - counts_before[k] for k in counts_after)
+    launch_kinds = {k: counts_after[k] - counts_before[k] for k in counts_after if counts_after[k] != counts_before[k]}
 
     value = world * n * args.steps / (total_ms / 1e3) / 1e9
     peak, peak_kind = measured_peak()
@@ -674,10 +679,9 @@ def run_gpu(args):
     s_out = torch.cuda.Stream(device=dev)
     done_cmp = [None] * len(chunks)          # compute of chunk c finished (grads free)
     done_out = [None] * len(chunks)          # params of chunk c copied out (params free)
-    launches_e2e = 0
 
     def e2e_steps(count, compute=True):
-        nonlocal t_global, launches_e2e
+        nonlocal t_global
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
         for _ in range(count):
@@ -695,7 +699,6 @@ def run_gpu(args):
                     stream.wait_event(done_out[c])
                 if compute:
                     asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
-                    launches_e2e += 1
                 ev_c = torch.cuda.Event()
                 ev_c.record(stream)
                 done_cmp[c] = ev_c
@@ -710,16 +713,18 @@ def run_gpu(args):
 
     e2e_steps(args.warmup)                   # untimed, like the device-resident leg
     torch.cuda.synchronize(dev)
-    launches_e2e = 0
     e_steps = max(1, args.steps)
     barrier()
+    e_counts_before = asr.asr_kernel_launches()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     e2e_steps(e_steps)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
+    e_counts_after = asr.asr_kernel_launches()
     barrier()
+    launches_e2e = sum(e_counts_after[k] - e_counts_before[k] for k in e_counts_after)
     require_no_device_error(asr.asr_take_device_error, "timed end-to-end steps")
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
@@ -762,7 +767,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": tpp * n if tpp is not None else None,
-                         "kernel": "adamw_sr_tma_kernel<bf16,bf16,SR,512>",
+                         "kernel": ("adamw_sr_tma_kernel<bf16,bf16,SR,512>" if "adamw_pipelined" in launch_kinds
+                                    else "adamw_sr_kernel<bf16,bf16,SR,vector,512>"),
                          "launch_ms_mean": launch_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * n,
@@ -778,6 +784,7 @@ def run_gpu(args):
                             "small_footprint_copies: the same bytes through a 512 MB page-locked "
                             "staging ring, no step calls)"},
             "gpu_launches": launches,
+            "gpu_launch_kinds": launch_kinds,
             "configs": others,
             "clocks": clock,
         }

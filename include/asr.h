@@ -38,13 +38,16 @@
  *     synchronising CUDA call of the caller.
  *   - n == 0 is a valid no-op (pointers may then be NULL).
  *   - The element-wise entry points (Philox, rounding, AdamW) accept any
- *     element alignment.  The AdamW step takes its pipelined path for every
- *     tensor whose buffers are 16-byte aligned, and for the part of a
+ *     element alignment.  The AdamW step takes 128-bit vector paths for
+ *     every tensor whose buffers are 16-byte aligned, and for the part of a
  *     tensor from its first element at which all four buffers are (the few
- *     elements before that take a scalar path); a base_index that is not a
- *     multiple of 4 costs one more Philox call per 8 elements, as it does
- *     on the rounding op's vectorised path.  The GEMM states its own
- *     requirements.
+ *     elements before that take scalar units): the pipelined kernel, except
+ *     that tensors launched together whose step moves at most 128 MiB (and
+ *     whose base indices are multiples of 4 where random bits are drawn)
+ *     take the register kernel, which starts faster.  A base_index that is
+ *     not a multiple of 4 costs one more Philox call per 8 elements, as it
+ *     does on the rounding op's vectorised path.  Every path gives the same
+ *     bits.  The GEMM states its own requirements.
  *   - Buffers of one call must not overlap each other (not checked).
  *   - The library is thread-safe; calls on different streams may run
  *     concurrently on disjoint buffers.  One exception:
@@ -53,9 +56,12 @@
  *   - CUDA graphs: asr_philox4x32, asr_stochastic_round_bf16,
  *     asr_adamw_sr_step, asr_adamw_sr_multi_tensor and asr_gemm_bf16_sr may
  *     be captured into a graph (stream capture) once a call of the same
- *     entry point has run on the device outside any capture -- that first
- *     call sets up the device's cached launch shapes -- and a replay gives
- *     the bits the direct calls give.  asr_take_device_error waits for its
+ *     entry point with work to do has run on the device outside any capture
+ *     -- that first call sets up the launch shapes of every kernel the entry
+ *     point may pick on that device (for the two AdamW entry points, of
+ *     both), so the captured calls need no set-up whatever their dtypes,
+ *     alignment and sizes -- and a replay gives the bits the direct calls
+ *     give.  asr_take_device_error waits for its
  *     stream and is not for capture; asr_take_device_error_async is.
  *   - The kernels are built for sm_103a (GB300) only; on any other GPU the
  *     first launch fails and the call returns ASR_ERR_CUDA.
@@ -265,6 +271,31 @@ asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream);
  * pointer (pageable host memory, NULL) returns ASR_ERR_INVALID_VALUE and
  * launches nothing. */
 asr_status asr_take_device_error_async(uint32_t *bits, asr_stream_t stream);
+
+/* Kinds of kernel launch counted by asr_kernel_launches. */
+typedef enum {
+    ASR_KERNEL_ADAMW_SCALAR = 0,             /* AdamW, register kernel, scalar units */
+    ASR_KERNEL_ADAMW_VECTOR = 1,             /* AdamW, register kernel, 128-bit units */
+    ASR_KERNEL_ADAMW_PIPELINED = 2,          /* AdamW, pipelined kernel, two counters per unit */
+    ASR_KERNEL_ADAMW_PIPELINED_ANY_BASE = 3, /* AdamW, pipelined kernel, three counters per unit */
+    ASR_KERNEL_ADAMW_STATIC = 4,             /* AdamW through asr_adamw_sr_multi_tensor_static */
+    ASR_KERNEL_ROUND = 5,                    /* asr_stochastic_round_bf16 */
+    ASR_KERNEL_PHILOX = 6,                   /* asr_philox4x32 */
+    ASR_KERNEL_GEMM = 7,                     /* asr_gemm_bf16_sr */
+    ASR_KERNEL_KINDS = 8
+} asr_kernel_kind;
+
+/* Diagnostic (no counterpart on the pages): copies into counts[k], for
+ * k < min(n, ASR_KERNEL_KINDS), how many kernels of kind k (asr_kernel_kind)
+ * the library has launched in this process -- on every device, stream and
+ * host thread, since it was loaded.  A launch is counted on the host when it
+ * has been queued without error, so a launch captured into a CUDA graph
+ * counts once and its replays do not.  Which AdamW kernel a step takes
+ * depends on its buffers' alignment, base indices and size (see the
+ * conventions above); these counters show which ones ran.  Makes no CUDA
+ * call.  counts may be NULL only when n == 0; n < 0 returns
+ * ASR_ERR_INVALID_VALUE. */
+asr_status asr_kernel_launches(uint64_t *counts, int32_t n);
 
 /* Diagnostic (no counterpart on the pages): launches one thread that waits,
  * with the kernels' bounded-wait routine and a limit of limit_ns

@@ -25,7 +25,11 @@ ASR_ROUND_SR, ASR_ROUND_RNE = 0, 1
 EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
            "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
            "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout",
-           "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr", "asr_take_device_error_async")
+           "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr", "asr_take_device_error_async",
+           "asr_kernel_launches")
+# asr_kernel_kind, in order
+KERNEL_KINDS = ("adamw_scalar", "adamw_vector", "adamw_pipelined", "adamw_pipelined_any_base", "adamw_static",
+                "round", "philox", "gemm")
 ASR_STATIC_TABLE_MAX = 4096
 
 
@@ -91,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.asr_take_device_error.restype = ctypes.c_int
         L.asr_take_device_error_async.argtypes = [vp, vp]
         L.asr_take_device_error_async.restype = ctypes.c_int
+        L.asr_kernel_launches.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
+        L.asr_kernel_launches.restype = ctypes.c_int
         L.asr_last_cuda_error.argtypes = []
         L.asr_last_cuda_error.restype = ctypes.c_int
         _lib = L
@@ -106,6 +112,15 @@ asr_status_string = status_string
 
 def asr_last_cuda_error() -> int:
     return int(lib().asr_last_cuda_error())
+
+
+def asr_kernel_launches() -> dict:
+    """Kernels the library has launched in this process, per kind (see
+    ``KERNEL_KINDS``): counted on the host when queued, on every device and
+    stream.  Makes no CUDA call."""
+    counts = (ctypes.c_uint64 * len(KERNEL_KINDS))()
+    _check(lib().asr_kernel_launches(counts, len(KERNEL_KINDS)), "asr_kernel_launches")
+    return dict(zip(KERNEL_KINDS, (int(c) for c in counts)))
 
 
 def asr_take_device_error(stream=None, device=None) -> int:

@@ -847,7 +847,7 @@ asr_status launch_pair(const CUtensorMap &ma, const CUtensorMap &mb, const CUten
     const uint64_t limit = kWaitLimitNs;
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_sr_pair_kernel<EPI>, ma, mb, mb_half, P, limit);
     if (e != cudaSuccess) return cuda_fail(e);
-    return check_launch();
+    return launched(ASR_KERNEL_GEMM);
 }
 
 // Row-major rows x k bf16 matrix, boxes of box_rows x 64 with 128-byte swizzle.
@@ -921,7 +921,7 @@ asr_status run(const uint16_t *a, const uint16_t *b, uint16_t *c, float *c_f32, 
     if (tiles >= (1ull << 31)) return ASR_ERR_INVALID_VALUE;
     const unsigned grid = static_cast<unsigned>(tiles < static_cast<uint64_t>(sms) ? tiles : sms);
     gemm_bf16_sr_kernel<<<grid, kThreads, kSmem, stream>>>(ma, mb, P, kWaitLimitNs);
-    return check_launch();
+    return launched(ASR_KERNEL_GEMM);
 }
 
 }  // namespace gemm

@@ -104,7 +104,7 @@ asr_status launch_static_group(int dev, const TensorEntry *dev_table, uint64_t t
     tab.t = dev_table;
     tab.total_tiles = tiles;
     kernel<<<grid, TmaShape<PT, GT>::kThreads, smem, stream>>>(tab, P, kWaitLimitNs);
-    return check_launch();
+    return launched(ASR_KERNEL_ADAMW_STATIC);
 }
 
 // Tensors whose buffers are not 16-byte aligned take the plain kernel, its
@@ -142,7 +142,7 @@ asr_status launch_static_plain(int dev, const asr_tensor_desc *table, int32_t n_
         g_stage_plain.count = c;
         const int g = static_cast<uint64_t>(grid) > tiles ? static_cast<int>(tiles) : grid;
         kernel<<<g, kThreads, 0, stream>>>(g_stage_plain, P);
-        asr_status st = check_launch();
+        asr_status st = launched(ASR_KERNEL_ADAMW_STATIC);
         if (st != ASR_OK) return st;
     }
     return ASR_OK;

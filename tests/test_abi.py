@@ -162,3 +162,21 @@ def test_gemm_rejects_bad_shapes_before_launching(L):
     assert g(ctypes.c_void_p(4097), p, p, None, 128, 128, 64, 0, 1, 0, None) == _lib.ASR_ERR_INVALID_VALUE
     assert g(p, p, p, None, 128, 128, 64, 7, 1, 0, None) == _lib.ASR_ERR_UNSUPPORTED_DTYPE
     assert g(None, None, None, None, 0, 128, 64, 0, 1, 0, None) == _lib.ASR_OK
+
+
+def test_launch_counters_read_without_a_gpu(L):
+    """asr_kernel_launches makes no CUDA call: it answers here, one counter
+    per asr_kernel_kind (none has moved: nothing is launched without a GPU),
+    fills at most ASR_KERNEL_KINDS entries and refuses a negative count."""
+    counts = asr.asr_kernel_launches()
+    assert list(counts) == list(_lib.KERNEL_KINDS) and all(v >= 0 for v in counts.values())
+    with open(os.path.join(ROOT, "include", "asr.h")) as f:
+        text = f.read()
+    kinds = re.search(r"ASR_KERNEL_KINDS\s*=\s*(\d+)", text)
+    assert kinds and int(kinds.group(1)) == len(_lib.KERNEL_KINDS)
+    buf = (ctypes.c_uint64 * 12)(*([7] * 12))
+    assert L.asr_kernel_launches(buf, 12) == _lib.ASR_OK
+    assert list(buf)[len(_lib.KERNEL_KINDS):] == [7] * (12 - len(_lib.KERNEL_KINDS))
+    assert L.asr_kernel_launches(None, 0) == _lib.ASR_OK
+    assert L.asr_kernel_launches(buf, -1) == _lib.ASR_ERR_INVALID_VALUE
+    assert L.asr_kernel_launches(None, 3) == _lib.ASR_ERR_INVALID_VALUE

@@ -36,11 +36,39 @@ def _make(rng, n, pdt, gdt, states=True, pscale=0.02, gscale=1e-3):
     return p, g, m, v
 
 
-def _step_both(asr, orc, h, d, **kw):
+# Steps of at most 128 MiB of traffic whose buffers are aligned (and whose
+# bases are multiples of 4, where bits are drawn) take the register kernel.
+# To put a small tensor through the pipelined kernel instead, a test steps
+# it in one multi-tensor call with a ballast tensor of the same dtypes that
+# takes the launch group past that size (its elements stay zero: p, g, m
+# and v all 0 give 0 again).
+BALLAST = 8_000_000
+_ballast_cache = {}
+
+
+def _ballast(pd, gd):
+    import torch
+    key = (pd.dtype, gd.dtype)
+    if key not in _ballast_cache:
+        _ballast_cache[key] = (torch.zeros(BALLAST, dtype=pd.dtype, device="cuda"),
+                               torch.zeros(BALLAST, dtype=gd.dtype, device="cuda"),
+                               torch.zeros(BALLAST, device="cuda"), torch.zeros(BALLAST, device="cuda"),
+                               2**36)
+    return _ballast_cache[key]
+
+
+def _step_both(asr, orc, h, d, via="alone", **kw):
+    """One step on the GPU and in the oracle.  via="alone": the tensor by
+    itself (asr_adamw_sr_step); via="pipelined": together with the ballast in
+    one multi-tensor call, so the tensor's launch group is large enough for
+    the pipelined kernel whatever its own size."""
     p, g, m, v = h
     pd, gd, md, vd = d
     base = kw.pop("base_index", 0)
-    asr.asr_adamw_sr_step(pd, gd, md, vd, base_index=base, **kw)
+    if via == "pipelined":
+        asr.asr_adamw_sr_multi_tensor([(pd, gd, md, vd, base), _ballast(pd, gd)], **kw)
+    else:
+        asr.asr_adamw_sr_step(pd, gd, md, vd, base_index=base, **kw)
     orc.adamw_step(p, g, m, v, base_index=base, rounding=0 if kw.get("rounding", "sr") == "sr" else 1,
                    **{k: val for k, val in kw.items() if k != "rounding"})
 
@@ -70,22 +98,65 @@ def test_single_tensor_65536_bf16_10_steps(asr, orc):
                                               ("bf16", "f32", "sr"), ("bf16", "f32", "rne"),
                                               ("f32", "bf16", "sr"), ("f32", "f32", "sr")])
 @pytest.mark.parametrize("base", [0, 5, 2**33 + 2, 2**40 + 3])
-def test_dtype_combinations_ragged(asr, orc, pdt, gdt, rounding, base):
+@pytest.mark.parametrize("via", ["alone", "pipelined"])
+def test_dtype_combinations_ragged(asr, orc, pdt, gdt, rounding, base, via):
     n = 3 * 4096 + 13
     rng = np.random.default_rng(hash((pdt, gdt, rounding, base)) % 2**32)
     h = _make(rng, n, pdt, gdt)
     d = [dev(a) for a in h]
     for step in (1, 2, 3):
-        _step_both(asr, orc, h, d, step=step, seed=2**40 + 17, base_index=base, rounding=rounding, **HP)
-        _check(h, d, f"{pdt}/{gdt}/{rounding} base {base} step {step}")
+        _step_both(asr, orc, h, d, via=via, step=step, seed=2**40 + 17, base_index=base, rounding=rounding, **HP)
+        _check(h, d, f"{pdt}/{gdt}/{rounding} base {base} step {step} {via}")
+
+
+def _kinds_launched(asr, fn):
+    """The library's kernel launches fn made, by kind (its launch counters)."""
+    before = asr.asr_kernel_launches()
+    fn()
+    after = asr.asr_kernel_launches()
+    return {k: after[k] - before[k] for k in after if after[k] != before[k]}
+
+
+def test_launch_group_size_picks_the_kernel(asr):
+    """Aligned tensors whose launch group moves at most 128 MiB take the
+    register kernel's vector units, larger groups (the ballast the tests use
+    included) the pipelined kernel; bf16 tensors at bases off a multiple of
+    4 take the pipelined kernel at any size; a view one element into its
+    storage is split into scalar units for its head and vector units for the
+    rest."""
+    import torch
+    rng = np.random.default_rng(31)
+    h = _make(rng, 65536, "bf16", "bf16")
+    d = [dev(a) for a in h]
+    assert _kinds_launched(asr, lambda: asr.asr_adamw_sr_step(*d, step=1, seed=0, **HP)) == {"adamw_vector": 1}
+    assert _kinds_launched(asr, lambda: asr.asr_adamw_sr_multi_tensor(
+        [(*d, 0), _ballast(d[0], d[1])], step=2, seed=0, **HP)) == {"adamw_pipelined": 1}
+    assert _kinds_launched(asr, lambda: asr.asr_adamw_sr_step(*d, base_index=3, step=3, seed=0, **HP)) == \
+        {"adamw_pipelined_any_base": 1}
+    views = [t[1:] for t in d]                 # first common aligned element: 7; base 1 + 7 = 8
+    assert _kinds_launched(asr, lambda: asr.asr_adamw_sr_step(*views, base_index=1, step=4, seed=0, **HP)) == \
+        {"adamw_scalar": 1, "adamw_vector": 1}
+    for pdt, gdt in (("f32", "f32"), ("bf16", "f32"), ("f32", "bf16")):
+        p = torch.zeros(65536, dtype=torch.float32 if pdt == "f32" else torch.bfloat16, device="cuda")
+        g = torch.zeros(65536, dtype=torch.float32 if gdt == "f32" else torch.bfloat16, device="cuda")
+        m, v = torch.zeros(65536, device="cuda"), torch.zeros(65536, device="cuda")
+        assert _kinds_launched(asr, lambda: asr.asr_adamw_sr_multi_tensor(
+            [(p, g, m, v, 0), _ballast(p, g)], step=1, seed=0, **HP)) == {"adamw_pipelined": 1}, (pdt, gdt)
+        # base 2: no bits drawn for f32 params; bf16 params need a multiple of 4
+        base = 2 if pdt == "f32" else 4
+        assert _kinds_launched(asr, lambda: asr.asr_adamw_sr_step(p, g, m, v, base_index=base, step=1, seed=0,
+                                                                  **HP)) == {"adamw_vector": 1}, (pdt, gdt)
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("off", [1, 2, 3])
-def test_unaligned_buffers(asr, orc, off):
+@pytest.mark.parametrize("via", ["alone", "pipelined"])
+def test_unaligned_buffers(asr, orc, off, via):
     """Buffers that start off a 16-byte boundary by the same element offset
     (slices) are split at the first element where all four are aligned: a
-    scalar head, then the pipelined kernel.  Bit-exact; nothing outside the
-    slice is written."""
+    scalar head, then the vector kernels (the register kernel alone, the
+    pipelined kernel in a large launch group).  Bit-exact; nothing outside
+    the slice is written."""
     import torch
     n = 4096 * 2 + 77
     rng = np.random.default_rng(off)
@@ -94,8 +165,8 @@ def test_unaligned_buffers(asr, orc, off):
     d = [t[off:] for t in full]
     hs = [a[off:].copy() for a in h]
     guard = [host(t)[:off].copy() for t in full]
-    _step_both(asr, orc, hs, d, step=4, seed=3, base_index=10 + off, **HP)
-    _check(hs, d, f"offset {off}")
+    _step_both(asr, orc, hs, d, via=via, step=4, seed=3, base_index=10 + off, **HP)
+    _check(hs, d, f"offset {off} {via}")
     for g0, t in zip(guard, full):
         assert np.array_equal(host(t)[:off], g0)
     torch.cuda.synchronize()
@@ -104,12 +175,14 @@ def test_unaligned_buffers(asr, orc, off):
 @pytest.mark.parametrize("pdt,gdt", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f32")])
 @pytest.mark.parametrize("offs", [(1, 1, 1, 1), (3, 3, 3, 3), (7, 7, 7, 7), (1, 3, 1, 1), (1, 1, 2, 2), (0, 0, 1, 1),
                                   (2, 2, 3, 3)])
-def test_unaligned_views(asr, orc, pdt, gdt, offs):
+@pytest.mark.parametrize("via", ["alone", "pipelined"])
+def test_unaligned_views(asr, orc, pdt, gdt, offs, via):
     """p, g, m, v each a view some elements into its storage, in every dtype
     combination: where some element puts all four on a 16-byte boundary the
-    tensor is split there (scalar head, pipelined rest), where none does it
-    takes the plain kernel -- either way bit-exact against the oracle, with
-    guard words before and after every view untouched."""
+    tensor is split there (scalar head, vector rest: alone, or in a launch
+    group large enough for the pipelined kernel), where none does it takes
+    the plain kernel's scalar units -- either way bit-exact against the
+    oracle, with guard words before and after every view untouched."""
     import torch
     rng = np.random.default_rng(sum(offs) + 7)
     n = 2 * 8192 + 45
@@ -121,8 +194,8 @@ def test_unaligned_views(asr, orc, pdt, gdt, offs):
         fulls.append((full, off))
         views.append(full[off:off + n])
     for base in (12, 13):
-        _step_both(asr, orc, h, views, step=2, seed=8, base_index=base, **HP)
-        _check(h, views, f"{pdt}/{gdt} offsets {offs} base {base}")
+        _step_both(asr, orc, h, views, via=via, step=2, seed=8, base_index=base, **HP)
+        _check(h, views, f"{pdt}/{gdt} offsets {offs} base {base} {via}")
     for full, off in fulls:
         t = host(full)
         assert np.all(t[:off] == 0x7E) and np.all(t[off + n:] == 0x7E), f"offsets {offs}: wrote outside the view"
@@ -137,7 +210,12 @@ TILE_EDGES = sorted({t * k + d for t in (3072, 4096, 5120, 6144, 8192) for k in 
 
 
 @pytest.mark.parametrize("pdt,gdt", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "bf16"), ("f32", "f32")])
-def test_small_and_boundary_sizes(asr, orc, pdt, gdt):
+@pytest.mark.parametrize("via", ["alone", "pipelined"])
+def test_small_and_boundary_sizes(asr, orc, pdt, gdt, via):
+    """Sizes 0-33 and the pipelined kernel's tile edges, bases 0, 1 and 3,
+    alone (the register kernel, or the pipelined one at bases off a
+    multiple of 4 with bits drawn) and in a launch group large enough for
+    the pipelined kernel; guard words after every buffer."""
     import torch
     rng = np.random.default_rng(11)
     sizes = list(range(0, 34)) if pdt == gdt == "bf16" else list(range(0, 34, 7))
@@ -147,8 +225,8 @@ def test_small_and_boundary_sizes(asr, orc, pdt, gdt):
             # guard bands after the buffers
             full = [dev(np.concatenate([a, np.full(9, 0x7E, a.dtype)])) for a in h]
             d = [t[:n] for t in full]
-            _step_both(asr, orc, h, d, step=2, seed=5, base_index=base, **HP)
-            _check(h, d, f"{pdt}/{gdt} n={n} base={base}")
+            _step_both(asr, orc, h, d, via=via, step=2, seed=5, base_index=base, **HP)
+            _check(h, d, f"{pdt}/{gdt} n={n} base={base} {via}")
             for t, a in zip(full, h):
                 assert np.all(host(t)[n:] == 0x7E), f"{pdt}/{gdt} n={n}: wrote past the end"
     torch.cuda.synchronize()
@@ -171,12 +249,13 @@ def test_special_values(asr, orc):
         m[:50] = 0.0
         if pdt == "bf16":
             p = W.to_bf16_bits(p)
-        h = [p, g, m, v]
-        d = [dev(a) for a in h]
-        for eps in (1e-8, 0.0):
-            _step_both(asr, orc, h, d, step=3, seed=8, lr=1e-2, beta1=0.9, beta2=0.999, eps=eps,
-                       weight_decay=0.1)
-            _check(h, d, f"specials {pdt} eps={eps}")
+        for via in ("alone", "pipelined"):
+            h = [a.copy() for a in (p, g, m, v)]
+            d = [dev(a) for a in h]
+            for eps in (1e-8, 0.0):
+                _step_both(asr, orc, h, d, via=via, step=3, seed=8, lr=1e-2, beta1=0.9, beta2=0.999, eps=eps,
+                           weight_decay=0.1)
+                _check(h, d, f"specials {pdt} eps={eps} {via}")
 
 
 def test_reproducible_and_keyed(asr):
@@ -464,19 +543,21 @@ def test_pipeline_matches_plain_path_every_step(asr, pdt, gdt, n, steps):
     dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=7, seed=2 ** 64 - 1),
 ], ids=["lr0", "betas0", "wd0", "step_max", "seed_max"])
 def test_degenerate_hyperparameters(asr, orc, case):
-    """The corners of the accepted hyperparameters, on both kernels (base 0
-    and base 3) with a ragged length, bit-exact against the oracle.  With
+    """The corners of the accepted hyperparameters, on every vector kernel
+    (base 0 alone: the register kernel; base 0 in a large launch group and
+    base 3: the pipelined kernel, two and three counters per unit) with a
+    ragged length, bit-exact against the oracle.  With
     lr = 0 the update is p * 1 - 0, so bf16 parameters come back unchanged
     under stochastic rounding (an exactly representable value has no bits to
     round) while the moments still move."""
     rng = np.random.default_rng(21)
     n = 3 * 5120 + 13
-    for base in (0, 3):
+    for base, via in ((0, "alone"), (0, "pipelined"), (3, "alone")):
         h = _make(rng, n, "bf16", "bf16")
         p0, m0 = h[0].copy(), h[2].copy()
         d = [dev(a) for a in h]
-        _step_both(asr, orc, h, d, base_index=base, **case)
-        _check(h, d, f"{case} base={base}")
+        _step_both(asr, orc, h, d, via=via, base_index=base, **case)
+        _check(h, d, f"{case} base={base} {via}")
         if case["lr"] == 0.0:
             assert np.array_equal(host(d[0]), p0), "lr = 0 changed a bf16 parameter"
             assert not np.array_equal(host(d[2]), m0), "lr = 0 must still update the first moment"

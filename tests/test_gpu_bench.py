@@ -30,6 +30,7 @@ def test_bench_native_arm_small():
                 "gpu_launches", "clocks"):
         assert key in d, key
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["gpu_launches"] == 3
+    assert d["gpu_launch_kinds"] == {"adamw_pipelined": 3}, d["gpu_launch_kinds"]
     assert 0 < d["config"]["params_per_gpu"] <= 20_000_000
     assert d["value"] > 0 and d["ms_per_step"] > 0
     roof = d["roofline"]

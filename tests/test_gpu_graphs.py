@@ -29,12 +29,20 @@ def _bits(t):
     return t.view(torch.int16) if t.dtype in (torch.bfloat16, torch.int16) else t.view(torch.int32)
 
 
-def _tensor_set(seed):
-    """Mixed tensors: aligned with bases that are multiples of 4 (pipelined
-    kernel), aligned with other bases (pipelined, three counters per unit),
-    one element off a 16-byte boundary (plain kernel)."""
+def _tensor_set(seed, large=False):
+    """Mixed tensors: aligned with bases that are multiples of 4 (the
+    register kernel's vector units while their launch group is small, the
+    pipelined kernel with `large`, which adds an 8M-param tensor to each such
+    group), aligned with other bases (pipelined, three counters per unit),
+    one element off a 16-byte boundary (scalar head, then vector units)."""
     rng = np.random.default_rng(seed)
     out, base = [], 0
+    if large:
+        for pdt in ("bf16", "f32"):
+            n = 8_000_000
+            p = np.zeros(n, np.uint16 if pdt == "bf16" else np.float32)
+            out.append(([p, np.zeros(n, np.uint16), np.zeros(n, np.float32), np.zeros(n, np.float32)], 0, base))
+            base += n
     for i in range(24):
         n = int(rng.integers(1, 30000))
         off = 1 if i % 5 == 4 else 0
@@ -53,9 +61,10 @@ def _device(hs):
     return [tuple(dev(a)[off:] for a in arrs) + (base,) for arrs, off, base in hs]
 
 
-def test_multi_tensor_step_in_a_graph(asr):
+@pytest.mark.parametrize("large", [False, True], ids=["small-groups", "large-groups"])
+def test_multi_tensor_step_in_a_graph(asr, large):
     import torch
-    hs = _tensor_set(3)
+    hs = _tensor_set(3, large)
     a, b = _device(hs), _device(hs)
     assert any(base % 4 for *_, base in a) and any(t[0].data_ptr() % 16 for t in a)
     for ts in (a, b):                          # first, ordinary call: sets up the caches
@@ -102,3 +111,49 @@ def test_rounding_philox_and_gemm_in_a_graph(asr):
     assert torch.equal(w_g, w_d)
     assert torch.equal(_bits(c_g), _bits(c_d))
     assert asr.asr_take_device_error() == 0
+
+
+_FIRST_USE = r"""
+import sys, torch
+sys.path.insert(0, ".")
+import stochastic_rounding_gb300 as asr
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+dev = torch.device("cuda", 0)
+def mk(n, pdt, gdt):
+    g = torch.Generator(device=dev); g.manual_seed(n)
+    return ((torch.randn(n, device=dev, generator=g) * 0.02).to(pdt), (torch.randn(n, device=dev, generator=g) * 1e-3).to(gdt),
+            torch.zeros(n, device=dev), torch.zeros(n, device=dev))
+small = mk(5000, torch.bfloat16, torch.bfloat16)
+asr.asr_adamw_sr_step(*small, step=1, seed=3, **HP)          # the only call before the capture
+big = [mk(7_000_000, torch.float32, torch.float32), mk(6_000_000, torch.bfloat16, torch.float32)]
+twin = [tuple(t.clone() for t in b) for b in big]
+s = torch.cuda.Stream(); s.wait_stream(torch.cuda.current_stream())
+graph = torch.cuda.CUDAGraph()
+with torch.cuda.graph(graph, stream=s):
+    asr.asr_adamw_sr_step(*big[0], step=2, seed=3, **HP)
+    asr.asr_adamw_sr_multi_tensor([(*big[1], 5)], step=2, seed=3, **HP)
+graph.replay()
+asr.asr_adamw_sr_step(*twin[0], step=2, seed=3, **HP)
+asr.asr_adamw_sr_multi_tensor([(*twin[1], 5)], step=2, seed=3, **HP)
+torch.cuda.synchronize()
+bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+for b, w in zip(big, twin):
+    for k in (0, 2, 3):
+        assert torch.equal(bits(b[k]), bits(w[k]))
+assert asr.asr_take_device_error() == 0
+print("FIRST_USE_OK")
+"""
+
+
+def test_capture_of_kernels_not_used_before(asr):
+    """In a fresh process, after one small bf16 step only, a capture holds
+    steps that take kernels no earlier call used (the f32 pipelined kernel,
+    the bf16/f32 kernel drawing three counters per unit): the first step on
+    a device sets up every AdamW kernel, so nothing is set up inside the
+    capture, and the replay gives the bits of direct calls."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_USE], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0 and "FIRST_USE_OK" in r.stdout, r.stderr[-3000:]
