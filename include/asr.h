@@ -207,10 +207,9 @@ asr_status asr_adamw_sr_multi_tensor(const asr_tensor_desc *table, int32_t n_ten
  *     anything is launched; otherwise the checks of the other entry points.
  *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
  *     routine; host staging uses fixed static buffers.
- *   - The first call on a device does that device's set-up (the array's
- *     device address, via cudaGetSymbolAddress with the device current, and
- *     the kernels' launch shapes); make that first call before any stream
- *     capture.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with the device current); the first call that
+ *     takes each of its kernels sets up that kernel's launch shape.
  *   - The table is copied into the array from the library's (pageable)
  *     host staging buffer with an asynchronous copy on `stream`: the runtime
  *     has taken the host bytes by the time the call returns, and the copy is
