@@ -225,7 +225,9 @@ asr_status validate_desc(const asr_tensor_desc &d)
 //     kernel with scalar units;
 //   kVecA4: 16-byte-aligned buffers and either a base index that is a
 //     multiple of 4 or no random bits needed (f32 params, nearest rounding)
-//     -- the pipelined kernel, two Philox counters per 8-element unit;
+//     -- the pipelined kernel, two Philox counters per 8-element unit, or,
+//     for a launch group of at most ASR_SMALL_GROUP_BYTES, the
+//     register-resident kernel with 128-bit units;
 //   kVecAnyBase: 16-byte-aligned buffers, stochastic rounding of bf16
 //     params, base index not a multiple of 4 -- the pipelined kernel drawing
 //     three counters per unit.  A model whose parameters are numbered end to
