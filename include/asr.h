@@ -271,6 +271,45 @@ asr_status asr_take_device_error(uint32_t *bits, asr_stream_t stream);
  * launches nothing. */
 asr_status asr_take_device_error_async(uint32_t *bits, asr_stream_t stream);
 
+/* A tensor for asr_adamw_sr_multi_tensor_host: its device buffers (dev: the
+ * step updates dev.param, dev.exp_avg and dev.exp_avg_sq in place and reads
+ * the gradient from dev.grad) and its host side: grad_host, n elements of
+ * dev.grad_dtype in page-locked host memory, copied into dev.grad before the
+ * step; param_host, n elements of dev.param_dtype in page-locked host
+ * memory that receives the updated parameters after the step, or NULL to
+ * leave them on the device only. */
+typedef struct {
+    asr_tensor_desc dev;
+    const void *grad_host;
+    void *param_host;
+} asr_host_tensor_desc;
+
+/* The multi-tensor step for callers whose gradients arrive in host memory
+ * and whose updated parameters go back to it (no counterpart on the pages:
+ * a runtime around the step).  The tensors, in table order, are grouped into
+ * chunks of consecutive tensors of at most chunk_elems elements (a larger
+ * tensor is a chunk of its own; chunk_elems 0 means 2^28); for each chunk
+ * the gradients are copied in on copy_in, the chunk's step runs on stream
+ * once they have arrived (bitwise the step asr_adamw_sr_multi_tensor gives
+ * the same descriptors), and its parameters are copied out on copy_out once
+ * its step is done, so that with three distinct non-blocking streams the
+ * copies of one chunk overlap the steps of its neighbours.  Ordering: all
+ * of it follows the work queued on `stream` before the call, and work queued
+ * on `stream` after the call follows all of it, copies included; copy_in
+ * and copy_out may be `stream` itself (no overlap then).  One copy per
+ * tensor and direction (cudaMemcpyAsync).  Host buffers must be page-locked
+ * (cudaHostAlloc / cudaMallocHost / cudaHostRegister; checked with
+ * cudaPointerGetAttributes -- any other pointer returns
+ * ASR_ERR_INVALID_VALUE before anything is queued) and stay valid and
+ * unchanged until the copies have run; the device gradient buffers must not
+ * be in use by other work.  The library keeps a pool of CUDA events per
+ * device for the ordering (created on first use, reused).  Host scratch: a
+ * descriptor array per call.  On ASR_ERR_CUDA part of the work may have been
+ * queued. */
+asr_status asr_adamw_sr_multi_tensor_host(const asr_host_tensor_desc *table, int32_t n_tensors,
+                                          const asr_adamw_hparams *hp, uint64_t chunk_elems,
+                                          asr_stream_t stream, asr_stream_t copy_in, asr_stream_t copy_out);
+
 /* Kinds of kernel launch counted by asr_kernel_launches. */
 typedef enum {
     ASR_KERNEL_ADAMW_SCALAR = 0,             /* AdamW, register kernel, scalar units */

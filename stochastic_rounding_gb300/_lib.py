@@ -26,7 +26,7 @@ EXPORTS = ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
            "asr_adamw_sr_step", "asr_adamw_sr_multi_tensor", "asr_status_string",
            "asr_last_cuda_error", "asr_take_device_error", "asr_selftest_wait_timeout",
            "asr_adamw_sr_multi_tensor_static", "asr_gemm_bf16_sr", "asr_take_device_error_async",
-           "asr_kernel_launches")
+           "asr_kernel_launches", "asr_adamw_sr_multi_tensor_host")
 # asr_kernel_kind, in order
 KERNEL_KINDS = ("adamw_scalar", "adamw_vector", "adamw_pipelined", "adamw_pipelined_any_base", "adamw_static",
                 "round", "philox", "gemm")
@@ -50,6 +50,10 @@ class TensorDesc(ctypes.Structure):
                 ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
                 ("n", ctypes.c_uint64), ("base_index", ctypes.c_uint64),
                 ("param_dtype", ctypes.c_int32), ("grad_dtype", ctypes.c_int32)]
+
+
+class HostTensorDesc(ctypes.Structure):
+    _fields_ = [("dev", TensorDesc), ("grad_host", ctypes.c_void_p), ("param_host", ctypes.c_void_p)]
 
 
 class AsrError(RuntimeError):
@@ -81,6 +85,9 @@ def lib() -> ctypes.CDLL:
                                                 ctypes.POINTER(AdamwHparams), vp]
         L.asr_adamw_sr_multi_tensor_static.argtypes = [ctypes.POINTER(TensorDesc), i32,
                                                        ctypes.POINTER(AdamwHparams), vp]
+        L.asr_adamw_sr_multi_tensor_host.argtypes = [ctypes.POINTER(HostTensorDesc), i32,
+                                                     ctypes.POINTER(AdamwHparams), u64, vp, vp, vp]
+        L.asr_adamw_sr_multi_tensor_host.restype = ctypes.c_int
         L.asr_gemm_bf16_sr.argtypes = [vp, vp, vp, vp, u64, u64, u64, u32, u32, u64, vp]
         L.asr_gemm_bf16_sr.restype = ctypes.c_int
         for f in ("asr_philox4x32", "asr_stochastic_round_bf16", "asr_adamw_prepare",
@@ -355,6 +362,65 @@ def asr_adamw_sr_multi_tensor(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, 
         _check(lib().asr_adamw_sr_multi_tensor(table, len(table), ctypes.byref(h),
                                                _stream_handle(dev, stream)),
                "asr_adamw_sr_multi_tensor")
+
+
+def _host_ptr(t, name, dtypes, numel):
+    """Address of a contiguous CPU tensor (page-locked memory: the library
+    checks that and refuses anything else)."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a CPU tensor in page-locked memory")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+    if not t.is_contiguous() or t.numel() != numel:
+        raise ValueError(f"{name} must be contiguous with {numel} elements")
+    return t.data_ptr()
+
+
+def make_host_table(tensors: Sequence[Sequence]) -> ctypes.Array:
+    """Descriptor array for ``asr_adamw_sr_multi_tensor_host`` from
+    (param, grad, exp_avg, exp_avg_sq, base_index, grad_host, param_host)
+    tuples: the first five as for ``make_table`` (CUDA tensors, one device),
+    grad_host a page-locked CPU tensor of grad's dtype and size, param_host one
+    of param's dtype and size or None."""
+    torch = _torch()
+    dev_table = make_table([t[:5] for t in tensors])
+    arr = (HostTensorDesc * len(tensors))()
+    for i, t in enumerate(tensors):
+        p, g, host_g, host_p = t[0], t[1], t[5], t[6]
+        same = lambda x: (torch.bfloat16, torch.int16) if x.dtype in (torch.bfloat16, torch.int16) else (x.dtype,)  # noqa: E731
+        gh = _host_ptr(host_g, f"grad_host[{i}]", same(g), g.numel())
+        ph = _host_ptr(host_p, f"param_host[{i}]", same(p), p.numel()) if host_p is not None else None
+        arr[i] = HostTensorDesc(dev_table[i], gh, ph)
+    return arr
+
+
+def asr_adamw_sr_multi_tensor_host(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step,
+                                   seed=0, rounding="sr", chunk_elems=0, stream=None, copy_in=None,
+                                   copy_out=None, device=None):
+    """The multi-tensor step with gradients copied in from page-locked host
+    memory and the updated parameters copied back to it, pipelined in the
+    library over chunks of consecutive tensors: copies in on ``copy_in``,
+    steps on ``stream``, copies out on ``copy_out`` (each defaulting to
+    ``stream``, which gives no overlap; pass two other streams for it).
+    ``tensors``: a table made by ``make_host_table`` (then ``device`` names the
+    CUDA device) or the tuples it takes."""
+    torch = _torch()
+    if isinstance(tensors, ctypes.Array):
+        table = tensors
+        dev = torch.device(device if device is not None else "cuda")
+    else:
+        table = make_host_table(tensors)
+        dev = tensors[0][0].device if len(tensors) else torch.device("cuda")
+    h = make_hparams(lr, beta1, beta2, eps, weight_decay, step, seed, rounding)
+    with _on_device(dev):
+        s = _stream_handle(dev, stream)
+        cin = _stream_handle(dev, copy_in) if copy_in is not None else s
+        cout = _stream_handle(dev, copy_out) if copy_out is not None else s
+        _check(lib().asr_adamw_sr_multi_tensor_host(table, len(table), ctypes.byref(h), int(chunk_elems), s, cin,
+                                                    cout), "asr_adamw_sr_multi_tensor_host")
 
 
 def asr_adamw_sr_multi_tensor_static(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1e-8,

@@ -180,3 +180,25 @@ def test_launch_counters_read_without_a_gpu(L):
     assert L.asr_kernel_launches(None, 0) == _lib.ASR_OK
     assert L.asr_kernel_launches(buf, -1) == _lib.ASR_ERR_INVALID_VALUE
     assert L.asr_kernel_launches(None, 3) == _lib.ASR_ERR_INVALID_VALUE
+
+
+def test_host_step_rejects_bad_arguments_before_any_cuda_call(L):
+    """asr_adamw_sr_multi_tensor_host: an empty table is a no-op, and a
+    missing or misaligned host gradient, a NULL table or bad hyperparameters
+    are refused before anything is queued (no GPU here)."""
+    h = _hp()
+    assert L.asr_adamw_sr_multi_tensor_host(None, 0, ctypes.byref(h), 0, None, None, None) == _lib.ASR_OK
+    assert L.asr_adamw_sr_multi_tensor_host(None, 2, ctypes.byref(h), 0, None, None, None) == \
+        _lib.ASR_ERR_INVALID_VALUE
+
+    def one(grad_host, param_host=None, n=8, gdt=_lib.ASR_BF16):
+        d = _lib.TensorDesc(16, 16, 16, 16, n, 0, _lib.ASR_BF16, gdt)
+        return (_lib.HostTensorDesc * 1)(_lib.HostTensorDesc(d, grad_host, param_host))
+
+    for t in (one(None), one(18, gdt=_lib.ASR_F32), one(16, 17)):
+        assert L.asr_adamw_sr_multi_tensor_host(t, 1, ctypes.byref(h), 0, None, None, None) == \
+            _lib.ASR_ERR_INVALID_VALUE
+    assert L.asr_adamw_sr_multi_tensor_host(one(None, n=0), 1, ctypes.byref(h), 0, None, None, None) == _lib.ASR_OK
+    bad = _hp(step=0)
+    assert L.asr_adamw_sr_multi_tensor_host(one(16), 1, ctypes.byref(bad), 0, None, None, None) == \
+        _lib.ASR_ERR_INVALID_VALUE
