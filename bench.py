@@ -42,6 +42,7 @@ KERNEL_SRC = [os.path.join(ROOT, "stochastic_rounding_gb300", "csrc", f)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 CPU_SAMPLE_ELEMS = 1 << 24     # oracle sample per step (one core)
+E2E_CHUNK = 1 << 28            # params per chunk of the end-to-end pipeline
 
 
 def require_no_device_error(take_error, region):
@@ -317,11 +318,11 @@ def ring_copies_seconds(g_dev, p_dev, n, dev, steps, chunk=1 << 26, slots=2):
     return seconds
 
 
-def e2e_chunks(tensors, offset, max_params=1 << 28):
-    """Consecutive tensors grouped into chunks of at most max_params (a larger
-    tensor is a chunk of its own).  Each chunk is a contiguous range [lo, hi)
-    of the flat buffers with its own descriptor table."""
-    from stochastic_rounding_gb300 import _lib
+def e2e_chunks(tensors, max_params=E2E_CHUNK):
+    """The chunks the end-to-end pipeline forms: consecutive tensors grouped
+    while they hold at most max_params (a larger tensor is a chunk of its
+    own), the rule asr_adamw_sr_multi_tensor_host applies.  Each chunk is the
+    contiguous range [lo, hi) of the flat buffers its tensors span."""
     groups, group, count = [], [], 0
     for t in tensors:
         n_t = t[0].numel()
@@ -332,12 +333,7 @@ def e2e_chunks(tensors, offset, max_params=1 << 28):
         count += n_t
     if group:
         groups.append(group)
-    res = []
-    for grp in groups:
-        lo = grp[0][4]
-        hi = grp[-1][4] + grp[-1][0].numel()
-        res.append((lo, hi, _lib.make_table([(p, g, m, v, base + offset) for p, g, m, v, base in grp])))
-    return res
+    return [(grp[0][4], grp[-1][4] + grp[-1][0].numel()) for grp in groups]
 
 
 def _oracle_shard_worker(args):
@@ -662,52 +658,55 @@ def run_gpu(args):
     achieved = BYTES_PER_PARAM * n / (launch_ms / 1e3) / 1e9
     tpp = traffic_per_param()
 
-    # ---- end to end through the C ABI with host buffers: every step copies
-    # the grads in from pinned host memory and the updated bf16 params back
-    # out.  Chunks of consecutive tensors (contiguous ranges of the flat
-    # buffers) are pipelined over three streams: H2D of chunk c+1 and D2H of
-    # chunk c-1 overlap the multi-tensor call on chunk c.
-    chunks = e2e_chunks(tensors, offset)
-    # one pinned host buffer per chunk: torch's pinned allocator rounds each
-    # request up to a power of two, which for two whole 16 GB buffers would
-    # double the host memory taken; per ~512 MB chunk the rounding wastes ~10 %
-    g_host = [torch.empty(hi - lo, dtype=torch.bfloat16, pin_memory=True) for lo, hi, _ in chunks]
-    p_host = [torch.empty(hi - lo, dtype=torch.bfloat16, pin_memory=True) for lo, hi, _ in chunks]
-    for (lo, hi, _), gh in zip(chunks, g_host):
+    # ---- end to end through the C ABI with host buffers: every step is one
+    # asr_adamw_sr_multi_tensor_host call, which copies the grads in from
+    # page-locked host memory, steps, and copies the updated bf16 params back
+    # out, pipelined in the library over chunks of consecutive tensors and
+    # three streams (copies of chunk c+1 in and c-1 out overlap the step on
+    # chunk c).
+    chunks = e2e_chunks(tensors)
+    # one pinned host buffer per chunk (a contiguous range [lo, hi) of the
+    # flat layout), each tensor a view of its chunk's buffer: torch's pinned
+    # allocator rounds each request up to a power of two, which for two whole
+    # 16 GB buffers would double the host memory taken; per ~512 MB chunk the
+    # rounding wastes ~10 %
+    g_host = [torch.empty(hi - lo, dtype=torch.bfloat16, pin_memory=True) for lo, hi in chunks]
+    p_host = [torch.empty(hi - lo, dtype=torch.bfloat16, pin_memory=True) for lo, hi in chunks]
+    for (lo, hi), gh in zip(chunks, g_host):
         gh.copy_(ps.g[lo:hi])
+    rows, c = [], 0
+    for p_t, g_t, m_t, v_t, base in tensors:
+        while base >= chunks[c][1]:
+            c += 1
+        a = base - chunks[c][0]
+        k = p_t.numel()
+        rows.append((p_t, g_t, m_t, v_t, base + offset, g_host[c][a:a + k], p_host[c][a:a + k]))
+    host_table = _lib.make_host_table(rows)
     s_in = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
-    done_cmp = [None] * len(chunks)          # compute of chunk c finished (grads free)
-    done_out = [None] * len(chunks)          # params of chunk c copied out (params free)
 
-    def e2e_steps(count, compute=True):
+    def e2e_steps(count):
         nonlocal t_global
+        for _ in range(count):
+            t_global += 1
+            asr.asr_adamw_sr_multi_tensor_host(host_table, step=t_global, seed=0, chunk_elems=E2E_CHUNK,
+                                               stream=stream, copy_in=s_in, copy_out=s_out, device=dev, **HP)
+        stream.wait_stream(s_out)            # the last params out are part of the step
+
+    def copies_steps(count):
+        """The same transfers with no step: per chunk, grads in on s_in and
+        params out on s_out after that chunk's grads are in."""
         s_in.wait_stream(stream)
         s_out.wait_stream(stream)
         for _ in range(count):
-            if compute:
-                t_global += 1
-            for c, (lo, hi, ctable) in enumerate(chunks):
-                ev_in = torch.cuda.Event()
+            for c, (lo, hi) in enumerate(chunks):
                 with torch.cuda.stream(s_in):
-                    if done_cmp[c] is not None:
-                        s_in.wait_event(done_cmp[c])
                     ps.g[lo:hi].copy_(g_host[c], non_blocking=True)
+                    ev_in = torch.cuda.Event()
                     ev_in.record(s_in)
-                stream.wait_event(ev_in)
-                if done_out[c] is not None:
-                    stream.wait_event(done_out[c])
-                if compute:
-                    asr.asr_adamw_sr_multi_tensor(ctable, step=t_global, seed=0, stream=stream, device=dev, **HP)
-                ev_c = torch.cuda.Event()
-                ev_c.record(stream)
-                done_cmp[c] = ev_c
                 with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_c)
+                    s_out.wait_event(ev_in)
                     p_host[c].copy_(ps.p[lo:hi], non_blocking=True)
-                    ev_o = torch.cuda.Event()
-                    ev_o.record(s_out)
-                done_out[c] = ev_o
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)
 
@@ -728,13 +727,12 @@ def run_gpu(args):
     require_no_device_error(asr.asr_take_device_error, "timed end-to-end steps")
     e_ms = max_over_ranks(e_start.elapsed_time(e_end))
     e2e_value = world * n * e_steps / (e_ms / 1e3) / 1e9
-    # the same pipeline with the step calls left out (copies and their
-    # ordering only), outside the timed region: what this machine's host link
-    # allows for the same transfers
+    # the same transfers with the steps left out, outside the timed region:
+    # what this machine's host link allows for them
     c_start = torch.cuda.Event(enable_timing=True)
     c_end = torch.cuda.Event(enable_timing=True)
     c_start.record(stream)
-    e2e_steps(e_steps, compute=False)
+    copies_steps(e_steps)
     c_end.record(stream)
     torch.cuda.synchronize(dev)
     copies_value = world * n * e_steps / (max_over_ranks(c_start.elapsed_time(c_end)) / 1e3) / 1e9
@@ -778,11 +776,12 @@ def run_gpu(args):
                     "frac_of_link_floor": e2e_value / world / (n / floor_s / 1e9),
                     "copies_only_gparams_s": copies_value, "frac_of_copies_only": e2e_value / copies_value,
                     "small_footprint_copies_gparams_s": ring_value,
-                    "what": "bf16 grads H2D from pinned host, step, bf16 params D2H to pinned host; "
-                            "chunks of consecutive tensors pipelined over three streams; host buffers "
-                            "hold the whole set (copies_only: the same pipeline without the step calls; "
+                    "what": "one asr_adamw_sr_multi_tensor_host call per step: bf16 grads H2D from "
+                            "pinned host, step, bf16 params D2H to pinned host, pipelined in the library "
+                            "over chunks of consecutive tensors and three streams; host buffers hold the "
+                            "whole set (copies_only: the same transfers per chunk without the steps; "
                             "small_footprint_copies: the same bytes through a 512 MB page-locked "
-                            "staging ring, no step calls)"},
+                            "staging ring, no steps)"},
             "gpu_launches": launches,
             "gpu_launch_kinds": launch_kinds,
             "configs": others,

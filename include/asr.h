@@ -294,10 +294,19 @@ typedef struct {
  * the same descriptors), and its parameters are copied out on copy_out once
  * its step is done, so that with three distinct non-blocking streams the
  * copies of one chunk overlap the steps of its neighbours.  Ordering: all
- * of it follows the work queued on `stream` before the call, and work queued
- * on `stream` after the call follows all of it, copies included; copy_in
- * and copy_out may be `stream` itself (no overlap then).  One copy per
- * tensor and direction (cudaMemcpyAsync).  Host buffers must be page-locked
+ * of it follows the work queued on `stream` before the call, and the steps
+ * also follow the work queued on copy_out before it (so a step never
+ * overwrites parameters that an earlier call is still copying out); work
+ * queued on `stream` after the call follows the steps -- and so the copies
+ * in: the host gradients may then be overwritten -- while the copies out
+ * complete on copy_out: wait on copy_out (an event recorded there after the
+ * call, or a synchronisation) before reading the host parameters.  Not
+ * joining copy_out back into `stream` lets one call's first copies in run
+ * while the previous call's last copies out finish.  copy_in and copy_out
+ * may be `stream` itself (no overlap then).  One copy
+ * (cudaMemcpyAsync) per tensor and direction, except that consecutive
+ * tensors of a chunk whose host and device ranges both follow on from one
+ * another are copied together.  Host buffers must be page-locked
  * (cudaHostAlloc / cudaMallocHost / cudaHostRegister; checked with
  * cudaPointerGetAttributes -- any other pointer returns
  * ASR_ERR_INVALID_VALUE before anything is queued) and stay valid and

@@ -405,6 +405,8 @@ def asr_adamw_sr_multi_tensor_host(tensors, *, lr, beta1=0.9, beta2=0.999, eps=1
     library over chunks of consecutive tensors: copies in on ``copy_in``,
     steps on ``stream``, copies out on ``copy_out`` (each defaulting to
     ``stream``, which gives no overlap; pass two other streams for it).
+    Later work on ``stream`` follows the steps; the host parameters are
+    ready once ``copy_out`` has reached the call's copies (wait on it).
     ``tensors``: a table made by ``make_host_table`` (then ``device`` names the
     CUDA device) or the tuples it takes."""
     torch = _torch()

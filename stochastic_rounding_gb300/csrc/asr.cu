@@ -662,19 +662,51 @@ asr_status run_adamw_host(const asr_host_tensor_desc *table, int32_t n_tensors, 
         give_events(dev, ev);
         return cuda_fail(err);
     };
-    // everything after the work already queued on `stream`
+    // everything after the work already queued on `stream`; the steps also
+    // after the copies out already queued on copy_out (an earlier call's
+    // copies out read the parameters these steps overwrite)
     if ((e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(cin, ev[0], 0)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamWaitEvent(cout, ev[0], 0)) != cudaSuccess) return fail(e);
+    if ((e = cudaEventRecord(ev.back(), cout)) != cudaSuccess) return fail(e);
+    if ((e = cudaStreamWaitEvent(stream, ev.back(), 0)) != cudaSuccess) return fail(e);
+    // Copies of consecutive tensors whose host and device ranges both follow
+    // on from the previous ones go out as one (the same bytes, fewer calls).
+    struct Pending {
+        char *dst = nullptr;
+        const char *src = nullptr;
+        size_t bytes = 0;
+    };
+    auto add = [](Pending &q, void *dst, const void *src, size_t bytes, cudaMemcpyKind kind,
+                  cudaStream_t s) -> cudaError_t {
+        char *d = static_cast<char *>(dst);
+        const char *r = static_cast<const char *>(src);
+        if (q.bytes && d == q.dst + q.bytes && r == q.src + q.bytes) {
+            q.bytes += bytes;
+            return cudaSuccess;
+        }
+        cudaError_t err = q.bytes ? cudaMemcpyAsync(q.dst, q.src, q.bytes, kind, s) : cudaSuccess;
+        q.dst = d;
+        q.src = r;
+        q.bytes = bytes;
+        return err;
+    };
+    auto flush = [](Pending &q, cudaMemcpyKind kind, cudaStream_t s) -> cudaError_t {
+        cudaError_t err = q.bytes ? cudaMemcpyAsync(q.dst, q.src, q.bytes, kind, s) : cudaSuccess;
+        q.bytes = 0;
+        return err;
+    };
     for (size_t c = 0; c < chunks.size(); ++c) {
         const int32_t first = chunks[c].first, last = chunks[c].second;
+        Pending in;
         for (int32_t i = first; i < last; ++i) {
             const asr_host_tensor_desc &h = table[i];
             if (h.dev.n == 0) continue;
             const size_t bytes = h.dev.n * (h.dev.grad_dtype == ASR_BF16 ? 2u : 4u);
-            e = cudaMemcpyAsync(const_cast<void *>(h.dev.grad), h.grad_host, bytes, cudaMemcpyHostToDevice, cin);
+            e = add(in, const_cast<void *>(h.dev.grad), h.grad_host, bytes, cudaMemcpyHostToDevice, cin);
             if (e != cudaSuccess) return fail(e);
         }
+        if ((e = flush(in, cudaMemcpyHostToDevice, cin)) != cudaSuccess) return fail(e);
         const cudaEvent_t arrived = ev[1 + 2 * c], stepped = ev[2 + 2 * c];
         if ((e = cudaEventRecord(arrived, cin)) != cudaSuccess) return fail(e);
         if ((e = cudaStreamWaitEvent(stream, arrived, 0)) != cudaSuccess) return fail(e);
@@ -685,17 +717,16 @@ asr_status run_adamw_host(const asr_host_tensor_desc *table, int32_t n_tensors, 
         }
         if ((e = cudaEventRecord(stepped, stream)) != cudaSuccess) return fail(e);
         if ((e = cudaStreamWaitEvent(cout, stepped, 0)) != cudaSuccess) return fail(e);
+        Pending out;
         for (int32_t i = first; i < last; ++i) {
             const asr_host_tensor_desc &h = table[i];
             if (h.dev.n == 0 || !h.param_host) continue;
             const size_t bytes = h.dev.n * (h.dev.param_dtype == ASR_BF16 ? 2u : 4u);
-            e = cudaMemcpyAsync(h.param_host, h.dev.param, bytes, cudaMemcpyDeviceToHost, cout);
+            e = add(out, h.param_host, h.dev.param, bytes, cudaMemcpyDeviceToHost, cout);
             if (e != cudaSuccess) return fail(e);
         }
+        if ((e = flush(out, cudaMemcpyDeviceToHost, cout)) != cudaSuccess) return fail(e);
     }
-    // work queued on `stream` after the call follows every copy out
-    if ((e = cudaEventRecord(ev.back(), cout)) != cudaSuccess) return fail(e);
-    if ((e = cudaStreamWaitEvent(stream, ev.back(), 0)) != cudaSuccess) return fail(e);
     give_events(dev, ev);
     return ASR_OK;
 }

@@ -79,7 +79,7 @@ def test_host_step_matches_the_oracle(asr, orc, streams):
             t["gh"].copy_(torch.from_numpy(g.view(np.int16) if g.dtype == np.uint16 else g))
         asr.asr_adamw_sr_multi_tensor_host(table, step=step, seed=2**34 + 1, chunk_elems=7_000, stream=s,
                                            copy_in=cin, copy_out=cout, device="cuda", **HP)
-        s.synchronize()
+        torch.cuda.synchronize()                       # the copies out complete on copy_out
         for t in ts:
             p, g, m, v = t["h"]
             orc.adamw_step(p, g, m, v, step=step, seed=2**34 + 1, base_index=t["base"], **HP)
@@ -95,9 +95,11 @@ def test_host_step_matches_the_oracle(asr, orc, streams):
 
 def test_host_step_orders_against_the_stream(asr):
     """Work queued on `stream` before the call is seen by it (the device
-    params it steps are set by a fill queued just before), and work queued
-    after it sees its results (a copy of the params queued right after on
-    `stream` holds the stepped values, equal to what went to the host)."""
+    params it steps are set by a fill queued just before), work queued on
+    `stream` after it sees the stepped params (a copy queued right after),
+    and once copy_out has been waited on the host holds the same values.
+    Two calls back to back on the same buffers (the second's steps follow
+    the first's copies out) give the host the second step's params."""
     import torch
     n = 300_000
     s = torch.cuda.Stream()
@@ -107,17 +109,25 @@ def test_host_step_orders_against_the_stream(asr):
     gh = torch.full((n,), 1e-3, dtype=torch.bfloat16, pin_memory=True)
     ph = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
     after = torch.empty_like(p)
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
     with torch.cuda.stream(s):
         p.fill_(0.5)
         asr.asr_adamw_sr_multi_tensor_host([(p, g, m, v, 0, gh, ph)], step=1, seed=5, chunk_elems=50_000,
-                                           stream=s, copy_in=torch.cuda.Stream(), copy_out=torch.cuda.Stream(),
-                                           **HP)
+                                           stream=s, copy_in=cin, copy_out=cout, **HP)
         after.copy_(p)
     s.synchronize()
-    assert torch.equal(after.view(torch.int16), p.view(torch.int16))
-    assert torch.equal(ph.view(torch.int16), after.cpu().view(torch.int16))
     assert float(after.float().mean()) < 0.5              # the step moved the params down from 0.5
     assert torch.equal(g.cpu().view(torch.int16), gh.view(torch.int16))
+    cout.synchronize()
+    assert torch.equal(ph.view(torch.int16), after.cpu().view(torch.int16))
+    table = asr.make_host_table([(p, g, m, v, 0, gh, ph)])
+    for step in (2, 3):
+        asr.asr_adamw_sr_multi_tensor_host(table, step=step, seed=5, chunk_elems=50_000, stream=s, copy_in=cin,
+                                           copy_out=cout, device="cuda", **HP)
+    with torch.cuda.stream(s):
+        after.copy_(p)
+    torch.cuda.synchronize()
+    assert torch.equal(ph.view(torch.int16), after.cpu().view(torch.int16))
 
 
 def test_host_step_refuses_pageable_memory(asr):
@@ -137,3 +147,57 @@ def test_host_step_refuses_pageable_memory(asr):
     assert asr.asr_kernel_launches() == before
     torch.cuda.synchronize()
     assert bool((p.float() == 0.25).all())
+
+
+def test_host_step_on_flat_buffers(asr, orc):
+    """Tensors laid end to end in flat host and device buffers (copies of a
+    run of them go out together), with one gap on the device side only and
+    one on the host side only (where a run must break), bf16 params and
+    grads: bitwise the oracle after two steps, on the device and in the host
+    copies, and the gap words untouched on both sides."""
+    import torch
+    rng = np.random.default_rng(77)
+    sizes = [4096, 1000, 333, 70_000, 8, 12_345, 4096, 2048, 999, 50_000, 16, 3]
+    dev_gap_after, host_gap_after = 4, 7          # tensor index followed by a 64-element gap
+    d_off, h_off, d, h = [], [], 0, 0
+    for i, n in enumerate(sizes):
+        d_off.append(d)
+        h_off.append(h)
+        d += n + (64 if i == dev_gap_after else 0)
+        h += n + (64 if i == host_gap_after else 0)
+    p = W.to_bf16_bits(W.normal_f32(rng, d, 0.02))
+    m = W.normal_f32(rng, d, 1e-4)
+    v = np.abs(W.normal_f32(rng, d, 1e-6))
+    p_d, m_d, v_d = dev(p), dev(m), dev(v)
+    g_d = dev(np.full(d, 0x7E7E, np.uint16))
+    g_h = torch.empty(h, dtype=torch.int16, pin_memory=True)
+    p_h = torch.full((h,), 0x5A5A, dtype=torch.int16, pin_memory=True)
+    rows, base = [], 0
+    for n, a, b in zip(sizes, d_off, h_off):
+        rows.append((p_d[a:a + n], g_d[a:a + n], m_d[a:a + n], v_d[a:a + n], base, g_h[b:b + n], p_h[b:b + n]))
+        base += n
+    table = asr.make_host_table(rows)
+    s, cin, cout = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    hp = [p.copy(), None, m.copy(), v.copy()]
+    for step in (1, 2):
+        g = W.to_bf16_bits(W.normal_f32(rng, h, 1e-3))
+        g_h.copy_(torch.from_numpy(g.view(np.int16)))
+        asr.asr_adamw_sr_multi_tensor_host(table, step=step, seed=9, chunk_elems=60_000, stream=s, copy_in=cin,
+                                           copy_out=cout, device="cuda", **HP)
+        torch.cuda.synchronize()
+        base = 0
+        for n, a, b in zip(sizes, d_off, h_off):
+            pp, mm, vv = hp[0][a:a + n].copy(), hp[2][a:a + n].copy(), hp[3][a:a + n].copy()
+            orc.adamw_step(pp, g[b:b + n].copy(), mm, vv, step=step, seed=9, base_index=base, **HP)
+            hp[0][a:a + n], hp[2][a:a + n], hp[3][a:a + n] = pp, mm, vv
+            base += n
+        got_p = host(p_d)
+        for i, (n, a, b) in enumerate(zip(sizes, d_off, h_off)):
+            assert_same_bits(got_p[a:a + n], hp[0][a:a + n], f"tensor {i} p step {step}")
+            assert_same_bits(host(m_d)[a:a + n], hp[2][a:a + n], f"tensor {i} m step {step}")
+            assert_same_bits(host(v_d)[a:a + n], hp[3][a:a + n], f"tensor {i} v step {step}")
+            assert np.array_equal(p_h.numpy()[b:b + n].view(np.uint16), hp[0][a:a + n]), f"tensor {i} host p"
+    gap_d = d_off[dev_gap_after] + sizes[dev_gap_after]
+    gap_h = h_off[host_gap_after] + sizes[host_gap_after]
+    assert np.all(host(g_d)[gap_d:gap_d + 64] == 0x7E7E), "device gap written"
+    assert np.all(p_h.numpy()[gap_h:gap_h + 64].view(np.uint16) == 0x5A5A), "host gap written"
