@@ -147,6 +147,37 @@ def test_gemm_many_tiles_per_cta(asr, orc):
     assert asr.asr_take_device_error() == 0
 
 
+@pytest.mark.parametrize("m,n,k,epilogue", [(2560, 2560, 768, 8), (2560, 2560, 1088, 4), (2816, 2560, 520, 8),
+                                             (2304, 2816, 136, 16), (2048, 2048, 2048, 16)])
+@pytest.mark.parametrize("rounding", ["sr", "rne"])
+def test_gemm_epilogue_widths(asr, orc, m, n, k, epilogue, rounding):
+    """Each epilogue width on the shapes that pick it: more pair tiles than
+    resident pairs (76 on GB300) take 8 warps for 512 < K <= 1024 and 4 above,
+    16 at K <= 512; every tile in one round (2048^2: 64 tiles) takes 16 at any
+    K.  The output equals the stand-alone rounding of the accumulator (itself
+    bit-exact with the oracle), the accumulator is within the bound, and
+    sampled rows match the oracle."""
+    import torch
+    a, b = _operands(m, n, k, seed=m + k)
+    c = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    acc = torch.empty(m, n, dtype=torch.float32, device="cuda")
+    asr.asr_gemm_bf16_sr(a, b, c, acc, rounding=rounding, step=6, seed=31)
+    ref = torch.empty(m * n, dtype=torch.int16, device="cuda")
+    if rounding == "sr":
+        asr.asr_stochastic_round_bf16(acc.view(-1), ref, base_index=0, step=6, seed=31)
+    else:
+        ref.copy_(acc.view(-1).to(torch.bfloat16).view(torch.int16))
+    torch.cuda.synchronize()
+    assert torch.equal(c.view(torch.int16).view(-1), ref), f"{m}x{n}x{k} ({epilogue} epilogue warps)"
+    _check_accumulator(a, b, acc)
+    rng = np.random.default_rng(m + n)
+    for i in rng.integers(0, m, 4):
+        row = host(acc[int(i)])
+        want = orc.sr_fill(row, int(i) * n, 6, 31) if rounding == "sr" else orc.rne_fill(row)
+        assert_same_bits(host(c[int(i)]), want, f"row {int(i)}", nan_equal=False)
+    assert asr.asr_take_device_error() == 0
+
+
 def test_one_sm_kernel_variant(asr, orc, tmp_path):
     """The one-SM 128 x 256 kernel, which the library falls back to where no
     CTA pair fits, built alone (-DASR_GEMM_PAIR=0) into a separate library:
