@@ -58,11 +58,21 @@ class AdamWSR(torch.optim.Optimizer):
     error bit: ``True``, ``"deferred"`` or ``False``; see the module notes).
     Parameters must be contiguous CUDA tensors of float32 or bfloat16;
     gradients dense float32 or bfloat16.
+
+    ``torch.optim.AdamW``'s other keywords are taken so that code written for
+    it runs unchanged: ``foreach``, ``fused`` and ``capturable`` are accepted
+    and have no effect (every step is one fused launch per group);
+    ``amsgrad``, ``maximize`` and ``differentiable`` are accepted when False
+    and refused otherwise (the fused step implements neither variant).
     """
 
     def __init__(self, params, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
-                 weight_decay: float = 1e-2, *, seed: int = 0, rounding: str = "sr",
-                 base_offset: int = 0, check_errors=True):
+                 weight_decay: float = 1e-2, amsgrad: bool = False, *, maximize: bool = False,
+                 foreach=None, capturable: bool = False, differentiable: bool = False, fused=None,
+                 seed: int = 0, rounding: str = "sr", base_offset: int = 0, check_errors=True):
+        for name, value in (("amsgrad", amsgrad), ("maximize", maximize), ("differentiable", differentiable)):
+            if value:
+                raise ValueError(f"AdamWSR does not support {name}=True")
         if not 0.0 <= lr:
             raise ValueError(f"Invalid learning rate: {lr}")
         if not 0.0 <= eps:

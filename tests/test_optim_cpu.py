@@ -125,3 +125,14 @@ def test_a_refused_parameter_leaves_every_group_unstepped(monkeypatch):
     refused.clear()
     opt.step()
     assert [s for _, s in fake.calls] == [1, 1] and opt.state[a]["step"] == 1
+
+
+def test_takes_torch_adamw_keywords():
+    """The keywords of torch.optim.AdamW are accepted where they change
+    nothing and refused where the fused step cannot honour them."""
+    p = torch.nn.Parameter(torch.zeros(4))
+    AdamWSR([p], 1e-3, (0.9, 0.999), 1e-8, 1e-2, False, maximize=False, foreach=True, capturable=True,
+            differentiable=False, fused=True)
+    for kw in (dict(amsgrad=True), dict(maximize=True), dict(differentiable=True)):
+        with pytest.raises(ValueError, match="does not support"):
+            AdamWSR([p], **kw)
