@@ -435,8 +435,56 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
         out[f"gemm_{m}x{n}x{k}"] = gemm_measure(asr, dev, m, n, k, steps, warmup, budget)
     out["sr_op_1073741824"] = elementwise_measure(asr, dev, "sr", 1 << 30, steps, warmup)
     out["philox_268435456"] = elementwise_measure(asr, dev, "philox", 1 << 28, steps, warmup)
+    out["subulp_demo"] = subulp_demo(asr, dev)
     torch.cuda.empty_cache()
     return out
+
+
+SUBULP_STEPS, SUBULP_LR, SUBULP_TARGET = 6000, 1e-4, 1.5
+
+
+def subulp_demo(asr, dev, n=65536):
+    """The pages' sub-ULP demonstration through the library: AdamW on the
+    loss (w - 1.5)^2 from w = 1.0, bf16 weights and no fp32 master copy, lr
+    1e-4 (a fortieth of the bf16 spacing below 1.0), 6,000 steps, for n
+    weights at once, with nearest and with stochastic rounding, and the
+    stochastic run repeated.  Reports the mean weights, whether nearest
+    rounding moved any weight, the same optimisation in binary64 without
+    rounding, and whether the rerun gave the same bits."""
+    import math
+    import time as _time
+
+    import torch
+    hp = dict(lr=SUBULP_LR, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+
+    def run(rounding):
+        w = torch.ones(n, dtype=torch.bfloat16, device=dev)
+        m = torch.zeros(n, device=dev)
+        v = torch.zeros(n, device=dev)
+        for k in range(1, SUBULP_STEPS + 1):
+            g = 2.0 * (w.float() - SUBULP_TARGET)
+            asr.asr_adamw_sr_step(w, g, m, v, step=k, seed=7, rounding=rounding, **hp)
+        torch.cuda.synchronize(dev)
+        return w
+
+    t0 = _time.time()
+    w_rn = run("rne")
+    w_sr = run("sr")
+    w_sr2 = run("sr")
+    seconds = _time.time() - t0
+    ref, m, v = 1.0, 0.0, 0.0
+    for k in range(1, SUBULP_STEPS + 1):
+        g = 2.0 * (ref - SUBULP_TARGET)
+        m = 0.9 * m + 0.1 * g
+        v = 0.999 * v + 0.001 * g * g
+        ref -= SUBULP_LR * (m / (1 - 0.9 ** k)) / (math.sqrt(v / (1 - 0.999 ** k)) + 1e-8)
+    require_no_device_error(asr.asr_take_device_error, "sub-ULP demonstration")
+    return {"what": "AdamW on (w - 1.5)^2 from w = 1.0, bf16 weights, no fp32 master, lr 1e-4, 6,000 steps",
+            "params": n, "steps": SUBULP_STEPS, "rn_mean": float(w_rn.float().mean()),
+            "rn_moved": bool((w_rn.float() != 1.0).any()), "sr_mean": float(w_sr.float().mean()),
+            "unrounded_binary64": ref, "sr_rerun_bitwise": bool(torch.equal(w_sr.view(torch.int16),
+                                                                            w_sr2.view(torch.int16))),
+            "seconds": seconds}
 
 
 def optimizer_step_time(asr, tensors, dev, steps, warmup, n):
