@@ -436,8 +436,37 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
     out["sr_op_1073741824"] = elementwise_measure(asr, dev, "sr", 1 << 30, steps, warmup)
     out["philox_268435456"] = elementwise_measure(asr, dev, "philox", 1 << 28, steps, warmup)
     out["subulp_demo"] = subulp_demo(asr, dev)
+    out["fp32_vs_torch_adamw"] = fp32_vs_torch_adamw(asr, W, dev)
     torch.cuda.empty_cache()
     return out
+
+
+def fp32_vs_torch_adamw(asr, W, dev, n=16_777_216, steps=100):
+    """The pages' accuracy criterion: fp32 parameters updated by the library
+    stay within 1e-4 of torch.optim.AdamW (its plain per-parameter form) run
+    on the same gradients, over 100 steps; n params ~N(0, 0.02), grads
+    ~N(0, 1e-3) drawn fresh every step.  Reports the largest absolute
+    difference at the end."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20240)
+    p = W.device_normal_(torch.empty(n, device=dev), gen, 0.02)
+    m = torch.zeros(n, device=dev)
+    v = torch.zeros(n, device=dev)
+    tp = torch.nn.Parameter(p.clone())
+    opt = torch.optim.AdamW([tp], lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                            weight_decay=HP["weight_decay"], foreach=False, fused=False)
+    g = torch.empty(n, device=dev)
+    for step in range(1, steps + 1):
+        W.device_normal_(g, gen, 1e-3)
+        asr.asr_adamw_sr_step(p, g, m, v, step=step, seed=0, **HP)
+        tp.grad = g
+        opt.step()
+    torch.cuda.synchronize(dev)
+    diff = float((p.double() - tp.detach().double()).abs().max())
+    require_no_device_error(asr.asr_take_device_error, "fp32 comparison with torch.optim.AdamW")
+    return {"what": "max |p - torch.optim.AdamW p| after 100 steps, fp32 params and grads, same grads",
+            "params": n, "steps": steps, "max_abs_diff": diff, "criterion": 1e-4, "within": diff < 1e-4}
 
 
 SUBULP_STEPS, SUBULP_LR, SUBULP_TARGET = 6000, 1e-4, 1.5
