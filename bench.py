@@ -437,8 +437,34 @@ def measure_configs(asr, W, dev, steps, warmup, peak):
     out["philox_268435456"] = elementwise_measure(asr, dev, "philox", 1 << 28, steps, warmup)
     out["subulp_demo"] = subulp_demo(asr, dev)
     out["fp32_vs_torch_adamw"] = fp32_vs_torch_adamw(asr, W, dev)
+    out["shard_invariance_268m"] = shard_invariance(asr, W, dev)
     torch.cuda.empty_cache()
     return out
+
+
+def shard_invariance(asr, W, dev, n=268_435_456, shards=8):
+    """The pages' shard invariance: one bf16 tensor of n params (~U(-1, 1)
+    params, ~N(0, 1e-2) grads, seed 1234, step 7) updated whole and as
+    `shards` contiguous shards (one of them cut off a multiple of 4, each
+    with its own base index), compared bit for bit."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    p = W.device_uniform_(torch.empty(n, device=dev), gen, -1.0, 1.0).to(torch.bfloat16)
+    g = W.device_normal_(torch.empty(n, device=dev), gen, 1e-2).to(torch.bfloat16)
+    whole = [p.clone(), g, torch.zeros(n, device=dev), torch.zeros(n, device=dev)]
+    split = [p, g, torch.zeros(n, device=dev), torch.zeros(n, device=dev)]
+    asr.asr_adamw_sr_step(*whole, base_index=0, step=7, seed=1234, **HP)
+    cuts = [n * k // shards for k in range(shards + 1)]
+    cuts[1] += 3                                   # one cut off a multiple of 4
+    asr.asr_adamw_sr_multi_tensor([(split[0][a:b], split[1][a:b], split[2][a:b], split[3][a:b], a)
+                                   for a, b in zip(cuts, cuts[1:])], step=7, seed=1234, **HP)
+    torch.cuda.synchronize(dev)
+    same = (torch.equal(whole[0].view(torch.int16), split[0].view(torch.int16))
+            and torch.equal(whole[2], split[2]) and torch.equal(whole[3], split[3]))
+    require_no_device_error(asr.asr_take_device_error, "shard invariance")
+    return {"what": "one 268M-param bf16 tensor updated whole and as 8 shards with their base indices",
+            "params": n, "shards": shards, "cuts": cuts, "bitwise_equal": bool(same)}
 
 
 def fp32_vs_torch_adamw(asr, W, dev, n=16_777_216, steps=100):
