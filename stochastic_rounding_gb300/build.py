@@ -15,7 +15,8 @@ SRC = os.path.join(HERE, "csrc", "asr.cu")
 HDR = os.path.join(ROOT, "include", "asr.h")
 # textually included by asr.cu (one translation unit)
 INCLUDED = [os.path.join(HERE, "csrc", f) for f in (
-    "common.cuh", "pipeline.cuh", "adamw_kernels.cuh", "rounding_kernels.cuh", "static_table.cuh", "gemm_sr.cuh")]
+    "common.cuh", "pipeline.cuh", "adamw_kernels.cuh", "rounding_kernels.cuh", "static_table.cuh",
+    "host_pipeline.cuh", "gemm_sr.cuh")]
 LIB = os.path.join(HERE, "libasr.so")
 
 NVCC_FLAGS = [
