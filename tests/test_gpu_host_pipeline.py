@@ -63,8 +63,10 @@ def _rows(ts):
     return [(t["d"][0], t["d"][1], t["d"][2], t["d"][3], t["base"], t["gh"], t["ph"]) for t in ts]
 
 
-@pytest.mark.parametrize("streams", ["three", "one"])
-def test_host_step_matches_the_oracle(asr, orc, streams):
+@pytest.mark.parametrize("streams,chunk", [("three", 7_000), ("one", 7_000), ("three", 1), ("three", 0)])
+def test_host_step_matches_the_oracle(asr, orc, streams, chunk):
+    """Chunks of ~7,000 params (one tensor is larger than that), of one
+    tensor each (chunk_elems 1), and all in one (0: the default 2^28)."""
     import torch
     ts = _set(41)
     s = torch.cuda.Stream()
@@ -77,7 +79,7 @@ def test_host_step_matches_the_oracle(asr, orc, streams):
             g = W.to_bf16_bits(g) if t["h"][1].dtype == np.uint16 else g
             t["h"][1] = g
             t["gh"].copy_(torch.from_numpy(g.view(np.int16) if g.dtype == np.uint16 else g))
-        asr.asr_adamw_sr_multi_tensor_host(table, step=step, seed=2**34 + 1, chunk_elems=7_000, stream=s,
+        asr.asr_adamw_sr_multi_tensor_host(table, step=step, seed=2**34 + 1, chunk_elems=chunk, stream=s,
                                            copy_in=cin, copy_out=cout, device="cuda", **HP)
         torch.cuda.synchronize()                       # the copies out complete on copy_out
         for t in ts:
