@@ -202,3 +202,24 @@ def test_host_step_rejects_bad_arguments_before_any_cuda_call(L):
     bad = _hp(step=0)
     assert L.asr_adamw_sr_multi_tensor_host(one(16), 1, ctypes.byref(bad), 0, None, None, None) == \
         _lib.ASR_ERR_INVALID_VALUE
+
+
+def test_header_compiles_as_c99_and_cxx(tmp_path):
+    """include/asr.h is a plain C header: a C99 translation unit (pedantic,
+    all warnings as errors) and a C++17 one that use its types compile."""
+    import shutil
+    import subprocess
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "asr.h"\n'
+                   "int main(void) {\n"
+                   "    asr_tensor_desc t; asr_host_tensor_desc h; asr_adamw_hparams hp; asr_adamw_scalars s;\n"
+                   "    (void)t; (void)h; (void)hp; (void)s;\n"
+                   "    return (int)ASR_KERNEL_KINDS + (int)ASR_STATIC_TABLE_MAX + (int)ASR_OK;\n"
+                   "}\n")
+    inc = os.path.join(ROOT, "include")
+    for cc, flags in (("gcc", ["-std=c99", "-pedantic"]), ("g++", ["-std=c++17", "-x", "c++"])):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not found")
+        r = subprocess.run([cc, *flags, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I", inc, str(src)],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, f"{cc}: {r.stderr}"
