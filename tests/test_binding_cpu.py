@@ -115,3 +115,58 @@ def test_tensors_on_another_device_are_refused_before_any_call(stub):
         _lib.asr_gemm_bf16_sr(_on(0, 4, 8, dtype=torch.bfloat16), _on(1, 4, 8, dtype=torch.bfloat16),
                               _on(0, 4, 4, dtype=torch.bfloat16))
     assert sum(fake.calls.values()) == 0
+
+
+def test_host_table_checks_its_host_tensors():
+    """make_host_table: the device parts as make_table checks them, the host
+    gradient of the gradient's dtype and size, the host params of the
+    params' dtype and size or None; CPU tensors only (page-locking is the
+    library's check)."""
+    import torch
+    p, g = _on(0, 8, dtype=torch.bfloat16), _on(0, 8, dtype=torch.float32)
+    m, v = _on(0, 8), _on(0, 8)
+    gh, ph = torch.zeros(8, dtype=torch.float32), torch.zeros(8, dtype=torch.int16)
+    t = _lib.make_host_table([(p, g, m, v, 3, gh, ph), (p, g, m, v, 11, gh, None)])
+    assert t[0].dev.base_index == 3 and t[0].grad_host == gh.data_ptr() and t[0].param_host == ph.data_ptr()
+    assert t[1].param_host is None
+    for bad_gh, bad_ph, err in ((torch.zeros(8, dtype=torch.bfloat16), ph, TypeError),
+                                (torch.zeros(7), ph, ValueError),
+                                (gh, torch.zeros(8), TypeError),
+                                (gh, torch.zeros(9, dtype=torch.bfloat16), ValueError),
+                                (_on(0, 8), ph, ValueError)):
+        with pytest.raises(err):
+            _lib.make_host_table([(p, g, m, v, 0, bad_gh, bad_ph)])
+
+
+def test_e2e_chunks_follow_the_library_rule():
+    """bench.e2e_chunks groups consecutive tensors while they hold at most
+    max_params (a larger tensor alone) -- the grouping the host-buffer step
+    applies -- into contiguous [lo, hi) ranges covering every tensor once."""
+    import bench
+
+    class T:
+        def __init__(self, n):
+            self.n = n
+
+        def numel(self):
+            return self.n
+
+    sizes = [5, 3, 9, 20, 1, 1, 6, 30, 2]
+    tensors, base = [], 0
+    for n in sizes:
+        tensors.append((T(n), None, None, None, base))
+        base += n + 2                            # a gap after each tensor
+    chunks = bench.e2e_chunks(tensors, max_params=10)
+    starts = [t[4] for t in tensors]
+    assert chunks[0][0] == 0 and chunks[-1][1] == starts[-1] + sizes[-1]
+    covered, i = [], 0
+    for lo, hi in chunks:
+        members = [k for k, s in enumerate(starts) if lo <= s < hi]
+        assert members and members[0] == i
+        total = sum(sizes[k] for k in members)
+        assert total <= 10 or len(members) == 1
+        if members[-1] + 1 < len(sizes):
+            assert total + sizes[members[-1] + 1] > 10          # a chunk stops only when the next would not fit
+        covered += members
+        i = members[-1] + 1
+    assert covered == list(range(len(sizes)))
