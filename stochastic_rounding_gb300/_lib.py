@@ -255,11 +255,16 @@ def _stream_handle(device, stream):
 _DTYPES = {}
 
 
-def _dt(t):
+def _dtype_codes():
+    """torch dtype -> asr_dtype code (bf16 patterns may come as int16)."""
     if not _DTYPES:
         torch = _torch()
         _DTYPES.update({torch.float32: ASR_F32, torch.bfloat16: ASR_BF16, torch.int16: ASR_BF16})
-    code = _DTYPES.get(t.dtype)
+    return _DTYPES
+
+
+def _dt(t):
+    code = _dtype_codes().get(t.dtype)
     if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
     return code
@@ -342,6 +347,27 @@ def make_table(tensors: Sequence[Sequence]) -> ctypes.Array:
             _dev_ptr(m, f"exp_avg[{i}]", (torch.float32,), n, dev),
             _dev_ptr(v, f"exp_avg_sq[{i}]", (torch.float32,), n, dev),
             n, int(base), _dt(p), _dt(g))
+    return arr
+
+
+# TensorDesc packed in one call (four 64-bit pointers, n, base_index, two
+# dtype codes; native alignment, no padding on the 64-bit hosts this runs on)
+_DESC_PACK = struct.Struct("=6Q2i")
+assert _DESC_PACK.size == ctypes.sizeof(TensorDesc)
+
+
+def _pack_table(entries) -> ctypes.Array:
+    """Descriptor array from (param, grad, exp_avg, exp_avg_sq, base_index)
+    tuples whose tensors the caller has already checked as ``make_table``
+    would (contiguous CUDA tensors on one device, matching sizes, supported
+    dtypes): the descriptors are packed without repeating the checks."""
+    arr = (TensorDesc * len(entries))()
+    codes = _dtype_codes()
+    off = 0
+    for p, g, m, v, base in entries:
+        _DESC_PACK.pack_into(arr, off, p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(), p.numel(), base,
+                             codes[p.dtype], codes[g.dtype])
+        off += _DESC_PACK.size
     return arr
 
 

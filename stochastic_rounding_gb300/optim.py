@@ -96,7 +96,6 @@ class AdamWSR(torch.optim.Optimizer):
                         seed=int(seed), rounding=rounding, base_index=None)
         super().__init__(params, defaults)
         self._assign_positions()
-        self._table_cache: Dict[tuple, object] = {}
 
     def _assign_positions(self):
         pos = self.base_offset
@@ -160,20 +159,22 @@ class AdamWSR(torch.optim.Optimizer):
         """Global parameter position of element 0 of ``p``."""
         return self._base[id(p)]
 
+    _DTYPES = frozenset((torch.float32, torch.bfloat16))
+
     @staticmethod
     def _check(p: torch.Tensor):
-        if p.device.type != "cuda":
+        if not p.is_cuda:
             raise ValueError("AdamWSR parameters must live on a CUDA device")
-        if p.dtype not in (torch.float32, torch.bfloat16):
+        if p.dtype not in AdamWSR._DTYPES:
             raise TypeError(f"AdamWSR supports float32 and bfloat16 parameters, not {p.dtype}")
         if not p.is_contiguous():
             raise ValueError("AdamWSR parameters must be contiguous")
         g = p.grad
         if g.is_sparse:
             raise RuntimeError("AdamWSR does not support sparse gradients")
-        if g.dtype not in (torch.float32, torch.bfloat16):
+        if g.dtype not in AdamWSR._DTYPES:
             raise TypeError(f"AdamWSR supports float32 and bfloat16 gradients, not {g.dtype}")
-        if not g.is_contiguous() or g.shape != p.shape or g.device != p.device:
+        if not g.is_contiguous() or g.shape != p.shape or g.get_device() != p.get_device():
             raise ValueError("gradient must be contiguous, on the parameter's device and of its shape")
 
     @torch.no_grad()
@@ -213,7 +214,7 @@ class AdamWSR(torch.optim.Optimizer):
                 batches.setdefault(key, []).append(
                     (p, p.grad, state["exp_avg"], state["exp_avg_sq"], self._base[id(p)]))
             for (device, step), entries in batches.items():
-                table = self._table(entries)
+                table = _lib._pack_table(entries)
                 _lib.asr_adamw_sr_multi_tensor(
                     table, lr=group["lr"], beta1=beta1, beta2=beta2, eps=group["eps"],
                     weight_decay=group["weight_decay"], step=step, seed=group["seed"],
@@ -229,19 +230,6 @@ class AdamWSR(torch.optim.Optimizer):
                     raise DeviceError(f"AdamWSR.step: device error bits {bits:#x} on {device} "
                                       "(a pipeline wait gave up; the step is incomplete)")
         return loss
-
-    def _table(self, entries):
-        """Descriptor table for these tensors, reused while every pointer,
-        size and dtype is unchanged (gradients are often reallocated)."""
-        key = tuple((p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(), p.numel(), base,
-                     p.dtype, g.dtype) for p, g, m, v, base in entries)
-        table = self._table_cache.get(key)
-        if table is None:
-            if len(self._table_cache) > 64:
-                self._table_cache.clear()
-            table = _lib.make_table(entries)
-            self._table_cache[key] = table
-        return table
 
     def load_state_dict(self, state_dict):
         """Like torch's, but the moments stay float32: torch's loader casts
@@ -262,4 +250,3 @@ class AdamWSR(torch.optim.Optimizer):
         for group in self.param_groups:
             group.setdefault("base_index", None)
         self._assign_positions()
-        self._table_cache.clear()

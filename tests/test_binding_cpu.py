@@ -170,3 +170,12 @@ def test_e2e_chunks_follow_the_library_rule():
         covered += members
         i = members[-1] + 1
     assert covered == list(range(len(sizes)))
+
+
+def test_packed_table_equals_the_checked_one():
+    """The optimizer's unchecked descriptor packing gives the same bytes as
+    make_table on the same tensors."""
+    import torch
+    rows = [(_on(0, 8, dtype=torch.bfloat16), _on(0, 8, dtype=torch.float32), _on(0, 8), _on(0, 8), 2**40 + 3),
+            (_on(0, 5), _on(0, 5, dtype=torch.bfloat16), _on(0, 5), _on(0, 5), 7)]
+    assert bytes(_lib._pack_table(rows)) == bytes(_lib.make_table(rows))

@@ -62,6 +62,8 @@ class _FakeLib:
     def make_table(self, entries):
         return [e[4] for e in entries]
 
+    _pack_table = make_table
+
     def asr_adamw_sr_multi_tensor(self, table, **kw):
         self.calls.append((list(table), kw["step"]))
 
