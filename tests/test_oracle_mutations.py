@@ -61,6 +61,11 @@ MUTATIONS = [
      "oracle_element_word(j * (row0 + m) + row0 + i, step, seed)", ["gemm"]),
     ("base_index ignored", "oracle_element_word(base_index + j, step, seed));\n            ((uint16_t",
      "oracle_element_word(j, step, seed));\n            ((uint16_t", ["dtype", "shards"]),
+    ("betas swapped in the second moment", "float bv = b2 * v;", "float bv = b1 * v;",
+     ["adamw", "adamw_special"]),
+    ("old second moment written back", "exp_avg_sq[j] = v1;", "exp_avg_sq[j] = v;", ["adamw", "adamw_special"]),
+    ("bias correction multiplied in", "float dq = rt / bc2s;", "float dq = rt * bc2s;", ["adamw", "adamw_special"]),
+    ("rounding modes swapped", "uint16_t h = rounding == 1", "uint16_t h = rounding == 0", ["dtype"]),
 ]
 
 
