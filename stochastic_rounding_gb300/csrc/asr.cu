@@ -511,29 +511,45 @@ asr_status run_adamw(const asr_tensor_desc *table, int32_t n_tensors, const asr_
     }
     int nt = 0;
     for (int32_t i = 0; i < n_tensors; ++i) nt += split_unaligned(table[i], rm, split + nt);
+    // one pass to classify, then a stable counting sort into the 12 groups
+    // (param dtype, grad dtype, class), each group in table order
+    constexpr int kGroups = 2 * 2 * 3;
     const asr_tensor_desc **sel = nullptr;
     const asr_tensor_desc *one[1];
+    int8_t group_small[8];
     std::unique_ptr<const asr_tensor_desc *[]> holder;
+    std::unique_ptr<int8_t[]> group_holder;
+    int8_t *group = group_small;
     if (nt <= 1) {
         sel = one;
     } else {
         holder.reset(new const asr_tensor_desc *[nt]);
         sel = holder.get();
     }
-    for (int pdt = 0; pdt < 2; ++pdt)
-        for (int gdt = 0; gdt < 2; ++gdt)
-            for (int cls = kPlainPath; cls <= kVecAnyBase; ++cls) {
-                int c = 0;
-                for (int i = 0; i < nt; ++i) {
-                    const asr_tensor_desc &d = split[i];
-                    if (d.n == 0 || d.param_dtype != pdt || d.grad_dtype != gdt || desc_class(d, rm) != cls)
-                        continue;
-                    sel[c++] = &d;
-                }
-                if (c == 0) continue;
-                st = dispatch(sel, c, pdt, gdt, rm, cls, P, stream);
-                if (st != ASR_OK) return st;
-            }
+    if (nt > 8) {
+        group_holder.reset(new int8_t[nt]);
+        group = group_holder.get();
+    }
+    int count[kGroups] = {}, start[kGroups];
+    for (int i = 0; i < nt; ++i) {
+        const asr_tensor_desc &d = split[i];
+        group[i] = d.n == 0 ? -1 : static_cast<int8_t>((d.param_dtype * 2 + d.grad_dtype) * 3 + desc_class(d, rm));
+        if (group[i] >= 0) ++count[group[i]];
+    }
+    for (int k = 0, at = 0; k < kGroups; ++k) {
+        start[k] = at;
+        at += count[k];
+    }
+    int fill[kGroups];
+    std::memcpy(fill, start, sizeof(fill));
+    for (int i = 0; i < nt; ++i)
+        if (group[i] >= 0) sel[fill[group[i]]++] = &split[i];
+    for (int k = 0; k < kGroups; ++k) {
+        if (count[k] == 0) continue;
+        const int pdt = k / 6, gdt = (k / 3) % 2, cls = k % 3;
+        st = dispatch(sel + start[k], count[k], pdt, gdt, rm, cls, P, stream);
+        if (st != ASR_OK) return st;
+    }
     return ASR_OK;
 }
 
