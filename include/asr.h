@@ -312,7 +312,8 @@ typedef struct {
  * ASR_ERR_INVALID_VALUE before anything is queued) and stay valid and
  * unchanged until the copies have run; the device gradient buffers must not
  * be in use by other work.  The library keeps a pool of CUDA events per
- * device for the ordering (created on first use, reused).  Host scratch: a
+ * device for the ordering (created on first use, reused; at most 4,096 kept
+ * per device, two per chunk are needed during a call).  Host scratch: a
  * descriptor array per call.  On ASR_ERR_CUDA part of the work may have been
  * queued. */
 asr_status asr_adamw_sr_multi_tensor_host(const asr_host_tensor_desc *table, int32_t n_tensors,

@@ -9,14 +9,22 @@
 // the host-buffer step.  A stream's wait on an event takes the event's state
 // when the wait is queued, so an event may go back to the pool as soon as its
 // record and its waits are queued.
+// The pool keeps at most kEventPoolMax events per device; a call that needed
+// more gives the rest back to the driver (destroying an event whose record or
+// waits are still pending is deferred by CUDA until they complete).
 constexpr int kEventDevices = 64;
+constexpr size_t kEventPoolMax = 4096;
 std::mutex g_event_mu;
 std::vector<cudaEvent_t> g_event_pool[kEventDevices];
 
 void give_events(int dev, std::vector<cudaEvent_t> &ev)
 {
     std::lock_guard<std::mutex> lk(g_event_mu);
-    g_event_pool[dev].insert(g_event_pool[dev].end(), ev.begin(), ev.end());
+    std::vector<cudaEvent_t> &pool = g_event_pool[dev];
+    for (cudaEvent_t e : ev) {
+        if (pool.size() < kEventPoolMax) pool.push_back(e);
+        else cudaEventDestroy(e);
+    }
     ev.clear();
 }
 

@@ -203,3 +203,39 @@ def test_host_step_on_flat_buffers(asr, orc):
     gap_h = h_off[host_gap_after] + sizes[host_gap_after]
     assert np.all(host(g_d)[gap_d:gap_d + 64] == 0x7E7E), "device gap written"
     assert np.all(p_h.numpy()[gap_h:gap_h + 64].view(np.uint16) == 0x5A5A), "host gap written"
+
+
+def test_host_step_with_more_chunks_than_the_event_pool_keeps(asr, orc):
+    """2,100 tensors of 1-9 params, one chunk each (4,202 events in one call,
+    above the 4,096 the pool keeps): bitwise the oracle after two calls."""
+    import torch
+    rng = np.random.default_rng(5)
+    rows, hosts, base = [], [], 0
+    for i in range(2100):
+        n = int(rng.integers(1, 10))
+        p = W.to_bf16_bits(W.normal_f32(rng, n, 0.02))
+        m = W.normal_f32(rng, n, 1e-4)
+        v = np.abs(W.normal_f32(rng, n, 1e-6))
+        d = (dev(p), dev(np.zeros(n, np.uint16)), dev(m), dev(v))
+        gh = torch.empty(n, dtype=torch.int16, pin_memory=True)
+        ph = torch.empty(n, dtype=torch.int16, pin_memory=True)
+        rows.append((*d, base, gh, ph))
+        hosts.append([p.copy(), None, m.copy(), v.copy(), base])
+        base += n
+    table = asr.make_host_table(rows)
+    s, cin, cout = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for step in (1, 2):
+        for r, h in zip(rows, hosts):
+            g = W.to_bf16_bits(W.normal_f32(rng, h[0].size, 1e-3))
+            h[1] = g
+            r[5].copy_(torch.from_numpy(g.view(np.int16)))
+        asr.asr_adamw_sr_multi_tensor_host(table, step=step, seed=3, chunk_elems=1, stream=s, copy_in=cin,
+                                           copy_out=cout, device="cuda", **HP)
+        torch.cuda.synchronize()
+        for h in hosts:
+            orc.adamw_step(h[0], h[1], h[2], h[3], step=step, seed=3, base_index=h[4], **HP)
+    for i, (r, h) in enumerate(zip(rows, hosts)):
+        assert np.array_equal(host(r[0]), h[0]), f"tensor {i} p"
+        assert np.array_equal(r[6].numpy().view(np.uint16), h[0]), f"tensor {i} host p"
+        assert np.array_equal(host(r[2]).view(np.uint32), h[2].view(np.uint32)), f"tensor {i} m"
+    assert asr.asr_take_device_error() == 0
